@@ -1,0 +1,191 @@
+// Internal structures of the mk library: the packed weight layout, the model
+// and step descriptors the persistent kernel reads, the shared-memory map and
+// the static work schedule of the skinny Q4 GEMM phases. Host and device code
+// of the library include it; nothing outside csrc/ does.
+#pragma once
+
+#include <cstdint>
+
+#include "mk.h"
+
+namespace mk {
+
+// ------------------------------------------------------------------ launch
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+
+// ------------------------------------------------------------- Q4 "units"
+// The GEMM phases stream weights as units of 32 output rows x 256 k
+// (one super-block column): 32 row headers of 16 bytes (binary16 d, binary16
+// dmin, the 12-byte 6-bit scale/min field, as in the canonical file), then
+// 4096 bytes of codes laid out so that each lane of a warp fetches, with one
+// 16-byte shared-memory load per sub-block, exactly the nibbles of its
+// m16n8k16 A fragments for both 16-row halves and both k-steps.
+constexpr int kUnitBytes = 4608;
+constexpr int kUnitHdr = 512;
+constexpr int kTileRows = 32;
+
+// Per-warp ring of streamed units (bulk async copies, mbarrier completion).
+constexpr int kRing = 3;
+
+// ----------------------------------------------------------- shared memory
+constexpr int kRingBytes = kWarps * kRing * kUnitBytes;   // 110592
+constexpr int kScaleTab = 2048;                           // [j8][g8][rb2][4 x u32]
+constexpr int kDTab = 128;                                // [g8][rb2][hi2] fp32
+constexpr int kWarpTab = kScaleTab + kDTab;               // 2176
+constexpr int kTabBytes = kWarps * kWarpTab;              // 17408
+constexpr int kActBytes = 96 * 1024;                      // activations / phase scratch
+constexpr int kMiscBytes = 4096;
+constexpr int kBarBytes = kWarps * kRing * 8;
+
+constexpr int kOffRing = 0;
+constexpr int kOffTab = kOffRing + kRingBytes;
+constexpr int kOffAct = kOffTab + kTabBytes;
+constexpr int kOffMisc = kOffAct + kActBytes;
+constexpr int kOffBar = kOffMisc + kMiscBytes;
+constexpr int kSmemBytes = kOffBar + kBarBytes;           // 229568
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
+// Attention and Gated DeltaNet phases may use the table and activation
+// regions together (they never hold a GEMM's data at that time).
+constexpr int kOffPhase = kOffTab;
+constexpr int kPhaseBytes = kTabBytes + kActBytes;        // 115712
+
+// --------------------------------------------------------------- limits
+constexpr int kMaxRows = MK_MAX_DECODE_ROWS;  // 12: at most 3 column tiles of 8
+constexpr int kMaxT = MK_MAX_T;
+constexpr int kMaxSeqs = MK_MAX_SEQS;
+constexpr int kMaxDh = 256;
+constexpr int kMaxQRows = 48;                 // T x (hq/hkv) rows attending one kv head
+
+// ------------------------------------------------------------- descriptors
+enum Prologue : int32_t { PRO_RMS_X = 0, PRO_GDN_OUT = 1, PRO_FA_OUT = 2, PRO_H = 3 };
+enum Epilogue : int32_t { EPI_STORE_YIN = 0, EPI_RESID_X = 1, EPI_SWIGLU_H = 2, EPI_TOP2 = 3 };
+
+struct GemmDesc {
+  const uint8_t* w;  // units [n_tiles][nsb]
+  int32_t n_tiles, nsb, n_out, pro, epi, pad;
+  const float* gain; // RMSNorm gain (PRO_RMS_X) or per-head output-norm gain (PRO_GDN_OUT)
+};
+
+struct LayerDesc {
+  int32_t kind, gdn_i, fa_i, pad;
+  GemmDesc in, o, gu, down;
+  const float* conv_w;  // [conv_ch][conv_w]
+};
+
+struct ModelDesc {
+  int32_t n_layers, H, F, V;
+  int32_t hq, hkv, dh, hk, hv, dk, dv, cw, conv_ch;
+  int32_t n_gdn, n_fa, n_in_max;      // y_in row stride
+  int32_t o_stride;                   // o row stride
+  int32_t kv_q8, page_tokens, n_pages, max_pages_per_seq, n_slots, max_seqs;
+  int32_t max_seg;                    // partial slots per warp per phase
+  int32_t grid;                       // blocks of the persistent launch
+  float eps;
+  LayerDesc layer[MK_MAX_LAYERS];
+  GemmDesc lm;
+  const float* final_norm;
+  const uint8_t* embed;               // canonical [V][H/256] super-blocks
+  // borrowed state
+  void* kv_k; void* kv_v; uint16_t* kv_ks; uint16_t* kv_vs;
+  float* gdn_state; float* conv_state;
+  // scratch
+  float* x;          // [kMaxRows][H] residual stream
+  float* yin;        // [kMaxRows][n_in_max] input projections
+  float* o;          // [kMaxRows][o_stride] mixer outputs
+  float* h;          // [kMaxRows][F] SwiGLU outputs
+  float* partial;    // [grid*kWarps][max_seg][kMaxRows][32]
+  uint32_t* tickets; // per tile
+  float* attn_part;  // [attn items][kMaxQRows][dh + 2]
+  uint32_t* attn_tickets;  // per (step sequence, kv head)
+  float* top_val;    // [grid*kWarps][kMaxRows]
+  int32_t* top_idx;  // [grid*kWarps][kMaxRows]
+  int32_t* page_table;     // [max_seqs][max_pages_per_seq]
+  int32_t* out;      // device result block (see kOut*)
+  uint32_t* bar;     // [0] arrivals, [1] generation
+  int32_t* err;      // [0] error code, [1] non-finite flag, [2] detail
+  float* dbg_logits; // optional
+  float* dbg_hidden; // optional
+};
+
+// Device result block layout.
+constexpr int kOutTokens = 0;                  // [kMaxRows]
+constexpr int kOutCounts = kMaxRows;           // [kMaxSeqs]
+constexpr int kOutArgmax = kMaxRows + kMaxSeqs;  // [kMaxRows]
+constexpr int kOutInts = kOutArgmax + kMaxRows;
+
+struct StepDesc {
+  int32_t R, n_seq, nt;               // rows, sequences, column tiles of 8
+  int32_t n_attn_items;
+  int32_t row_tok[kMaxRows], row_pos[kMaxRows], row_si[kMaxRows];
+  int32_t seq_id[kMaxSeqs], seq_row0[kMaxSeqs], seq_T[kMaxSeqs], seq_len[kMaxSeqs];
+  int32_t seq_slot_in[kMaxSeqs], seq_snap_all[kMaxSeqs];
+  int32_t seq_slot_out[kMaxSeqs][kMaxT];
+  int32_t seq_nsplit[kMaxSeqs], seq_tiles_per_split[kMaxSeqs], seq_item0[kMaxSeqs];
+  int32_t skip_block, skip_barrier;
+  uint64_t barrier_timeout_ns;
+  float2 rope[kMaxRows][kMaxDh / 2];  // (cos, sin) of position * base^(-2i/dh)
+};
+
+// Error codes in err[0] (device side), mapped to mk_status by the host.
+enum : int32_t { DEV_OK = 0, DEV_BARRIER_TIMEOUT = 1, DEV_COPY_TIMEOUT = 2, DEV_BAD_STATE = 3 };
+
+// Source rows of one packed phase matrix: up to four canonical matrices
+// stacked vertically, or (interleave_gate_up) the FFN gate and up matrices
+// interleaved in blocks of 8 rows.
+struct PackSrc {
+  int32_t n_seg;
+  int32_t row_begin[4], row_end[4];
+  const uint8_t* src[4];
+  int32_t interleave_gate_up;
+};
+
+// ------------------------------------------------------ GEMM work schedule
+// Every block computes the same schedule for a phase from (tiles, sb, rows,
+// grid): the reduction dimension is cut into S slices so that one slice of
+// activations (2 fp16 columns per row: high and low halves) fits in the
+// activation region; blocks are divided evenly among slices; inside a slice
+// the units (tile-major, super-block-minor) are divided evenly among warps.
+struct Sched {
+  int32_t S, sb_per;
+};
+
+__host__ __device__ inline int act_col_stride(int nsb_slice) { return nsb_slice * 512 + 64; }
+
+__host__ __device__ inline int act_bytes(int nsb_slice, int R) {
+  return 2 * R * act_col_stride(nsb_slice) + nsb_slice * 8 * R * 4;
+}
+
+__host__ __device__ inline Sched make_sched(int nsb, int R) {
+  Sched s;
+  int max_sb = 1;
+  while (max_sb < nsb && act_bytes(max_sb + 1, R) <= kActBytes) ++max_sb;
+  s.S = (nsb + max_sb - 1) / max_sb;
+  s.sb_per = (nsb + s.S - 1) / s.S;
+  return s;
+}
+
+__host__ __device__ inline int slice_sb0(const Sched& s, int sl) { return sl * s.sb_per; }
+__host__ __device__ inline int slice_nsb(const Sched& s, int nsb, int sl) {
+  int b = sl * s.sb_per, e = b + s.sb_per;
+  if (e > nsb) e = nsb;
+  return e - b;
+}
+__host__ __device__ inline int slice_cta0(const Sched& s, int grid, int sl) {
+  return (int)((int64_t)sl * grid / s.S);
+}
+__host__ __device__ inline int slice_of_cta(const Sched& s, int grid, int cta) {
+  // largest sl with slice_cta0(sl) <= cta
+  int sl = (int)(((int64_t)(cta + 1) * s.S - 1) / grid);
+  return sl;
+}
+// Units [u0, u1) of slice-local warp ws out of Ws warps over Us units.
+__host__ __device__ inline int64_t warp_u0(int64_t Us, int64_t Ws, int64_t ws) {
+  return ws * Us / Ws;
+}
+// Slice-local warp whose range holds unit u.
+__host__ __device__ inline int64_t warp_of_unit(int64_t Us, int64_t Ws, int64_t u) {
+  return ((u + 1) * Ws - 1) / Us;
+}
+
+}  // namespace mk

@@ -1,0 +1,177 @@
+"""Shared set-up for the GPU parity tests: one workload, the oracle and the
+CUDA engine started from identical seeded inputs, and the comparison rules.
+
+Tolerances (the verify step's stated parity bar):
+  logits         max |gpu - oracle| <= 2e-2 * rms(oracle logits) per row
+  hidden, state  relative L2 <= 1e-3
+  tokens, counts, page tables: exact, except rows whose oracle top-2 logit gap
+                 is below 1e-3 * rms(logits) (and every later row of that
+                 sequence), which are counted and reported
+  KV codes       new positions: q8 codes within 1 (exact on identical fp32
+                 inputs), fp16 within one binary16 step plus 1e-4 * rms; counted
+"""
+from __future__ import annotations
+
+import copy
+
+import numpy as np
+
+from gen import configs
+from gen.workload import Workload
+from oracle import oracle as orc
+
+LOGIT_TOL = 2e-2
+REL_L2_TOL = 1e-3
+TIE_GAP = 1e-3
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+class Pair:
+    def __init__(self, name="tiny", norm_jitter=0.1, overrides=None, nthreads=4, **kw):
+        import torch
+        from speculative_decode_persistent_gb300 import mk
+        self.torch = torch
+        self.wl = Workload(name, norm_jitter=norm_jitter, overrides=overrides, nthreads=nthreads, **kw)
+        wl = self.wl
+        self.orc_pool = copy.deepcopy(wl.pool)
+        self.oracle = orc.Oracle(wl.model, wl.weights, self.orc_pool, wl.kv_q8, wl.n_pages, wl.max_seqs,
+                                 nthreads=nthreads)
+        self.eng = mk.Engine(wl.model, wl.weights, wl.kv_q8, wl.n_pages, max_seqs=wl.max_seqs)
+        self.eng.load_pool(wl.pool)
+        for s, (cached, _T) in enumerate(wl.seqs):
+            S, conv = wl.states[s]
+            self.oracle.seq_set(s, cached, wl.tables[s], S, conv)
+            self.eng.seq_set(s, cached, wl.tables[s], S, conv)
+        V, H = wl.model["vocab"], wl.model["hidden"]
+        self.logits = torch.zeros((12, V), dtype=torch.float32, device="cuda")
+        self.hidden = torch.zeros((12, H), dtype=torch.float32, device="cuda")
+        self.eng.debug_outputs(self.logits, self.hidden)
+
+    def step(self, tokens, positions, seq_ids):
+        ro = self.oracle.step(tokens, positions, seq_ids, want_logits=True, want_hidden=True)
+        gt, gc = self.eng.step(tokens, positions, seq_ids)
+        R = len(tokens)
+        gl = self.logits[:R].double().cpu().numpy()
+        gh = self.hidden[:R].double().cpu().numpy()
+        return ro, dict(tokens=gt, counts=gc, logits=gl, hidden=gh)
+
+    def compare_step(self, ro, rg, seq_ids):
+        """Returns (n_excused_rows, report dict); asserts the parity bar."""
+        R = len(seq_ids)
+        rep = dict(max_logit_err_over_rms=0.0, hidden_rel_l2=0.0)
+        for r in range(R):
+            rms = ro["rms"][r]
+            err = float(np.max(np.abs(rg["logits"][r] - ro["logits"][r])))
+            rep["max_logit_err_over_rms"] = max(rep["max_logit_err_over_rms"], err / rms)
+            assert err <= LOGIT_TOL * rms, f"row {r}: logits err {err} > {LOGIT_TOL} * rms {rms}"
+            h = rel_l2(rg["hidden"][r], ro["hidden"][r])
+            rep["hidden_rel_l2"] = max(rep["hidden_rel_l2"], h)
+            assert h <= REL_L2_TOL, f"row {r}: hidden rel L2 {h}"
+        # tokens and counts per sequence, with near-tie excusal
+        order = []
+        for s in seq_ids:
+            if not order or order[-1] != s:
+                order.append(int(s))
+        excused = 0
+        at_o = at_g = 0
+        row = 0
+        for i, s in enumerate(order):
+            T = int(np.sum(np.asarray(seq_ids) == s))
+            co, cg = int(ro["counts"][i]), int(rg["counts"][i])
+            tie_rows = [j for j in range(T) if ro["gap"][row + j] < TIE_GAP * ro["rms"][row + j]]
+            first_tie = min(tie_rows) if tie_rows else T
+            if first_tie < co:  # the verify outcome may legitimately differ
+                excused += T - first_tie
+            else:
+                assert cg == co, f"seq {s}: count gpu {cg} oracle {co}"
+                assert np.array_equal(rg["tokens"][at_g:at_g + cg], ro["tokens"][at_o:at_o + co]), \
+                    f"seq {s}: tokens gpu {rg['tokens'][at_g:at_g + cg]} oracle {ro['tokens'][at_o:at_o + co]}"
+            at_o += co
+            at_g += cg
+            row += T
+        rep["excused_rows"] = excused
+        return excused, rep
+
+    def compare_state(self, seq):
+        so = self.oracle.seq_get(seq)
+        sg = self.eng.seq_get(seq)
+        assert so["length"] == sg["length"], (so["length"], sg["length"])
+        assert np.array_equal(so["pages"], sg["pages"]), (so["pages"], sg["pages"])
+        S = sg["S"].double().cpu().numpy()
+        C = sg["conv"].double().cpu().numpy()
+        es, ec = rel_l2(S, so["S"]), rel_l2(C, so["conv"])
+        assert es <= REL_L2_TOL, f"seq {seq}: GDN state rel L2 {es}"
+        assert ec <= REL_L2_TOL, f"seq {seq}: conv state rel L2 {ec}"
+        return dict(state_rel_l2=es, conv_rel_l2=ec)
+
+    def compare_kv(self, seq, positions):
+        """New positions of one sequence in every attention layer.
+
+        fp16 pool: decoded values within one binary16 step of the element
+        (2^-10 |x|) plus 1e-4 * rms of the stored head vector (the inputs differ
+        by fp32-vs-fp64 rounding, so an element on a rounding boundary lands one
+        step away and near-zero elements a few steps). q8 pool: codes within 1
+        and scales within one binary16 step. Returns the number of differing
+        elements."""
+        views = self.eng.kv_views()
+        table = self.oracle.seq_get(seq)["pages"]
+        diffs = 0
+        for name, v in views.items():
+            g = v.cpu().numpy()
+            o = self.orc_pool[name].view(g.dtype)
+            for p in positions:
+                page, slot = table[p // 16], p % 16
+                gg, oo = g[:, page, :, slot], o[:, page, :, slot]
+                if name in ("k", "v"):
+                    gf = gg.view(np.float16).astype(np.float64)
+                    of = oo.view(np.float16).astype(np.float64)
+                    rms = np.sqrt(np.mean(of ** 2, axis=-1, keepdims=True))
+                    err = np.abs(gf - of)
+                    bound = 2.0 ** -10 * np.abs(of) + 1e-4 * rms + 1e-30
+                    assert np.all(err <= bound), f"{name}: max err/bound {np.max(err / bound)}"
+                    d = gg != oo
+                else:
+                    d = np.abs(gg.astype(np.int32) - oo.astype(np.int32))
+                    assert d.max() <= 1, f"{name} differs by {d.max()}"
+                diffs += int(np.count_nonzero(d))
+        return diffs
+
+
+def greedy_continuation(name, n, seq=0, norm_jitter=0.1, overrides=None, nthreads=4):
+    """Oracle greedy tokens after the first row token of sequence `seq`,
+    by single-row passes (drafts for the verify tests)."""
+    wl = Workload(name, norm_jitter=norm_jitter, overrides=overrides, nthreads=nthreads)
+    o = orc.Oracle(wl.model, wl.weights, wl.pool, wl.kv_q8, wl.n_pages, wl.max_seqs, nthreads=nthreads)
+    for s, (cached, _T) in enumerate(wl.seqs):
+        o.seq_set(s, cached, wl.tables[s], *wl.states[s])
+    tok = int(wl.first_tokens[seq])
+    pos = wl.seqs[seq][0]
+    out = []
+    for j in range(n):
+        r = o.step([tok], [pos + j], [seq])
+        o.commit([seq], [1])
+        tok = int(r["argmax"][0])
+        out.append(tok)
+    return out
+
+
+def drafts_with_mismatch(greedy, T, m, vocab, salt=0):
+    """Drafts d_1..d_{T-1} equal to the greedy continuation up to index m,
+    then one wrong token, so that exactly m drafts are accepted."""
+    d = []
+    for i in range(1, T):
+        if i <= m:
+            d.append(greedy[i - 1])
+        elif i == m + 1:
+            d.append((greedy[i - 1] + 1 + 7 * salt) % vocab)
+        else:
+            d.append((greedy[i - 1] * 31 + 5 + salt) % vocab)
+    return d
+
+
+__all__ = ["Pair", "greedy_continuation", "drafts_with_mismatch", "rel_l2", "configs"]
