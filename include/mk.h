@@ -259,6 +259,30 @@ mk_status mk_step_io_bytes(mk_ctx* ctx, uint64_t* h2d_bytes, uint64_t* d2h_bytes
 /* Number of grid blocks of the persistent launch (SM count x blocks per SM). */
 int32_t mk_grid_blocks(mk_ctx* ctx);
 
+/*
+ * Allocation-free step (no counterpart on the pages: a deployment aid).
+ * For callers that cannot allocate device memory when they step — code
+ * running while a CUDA graph is being captured, or inside a memory pool or
+ * allocator that must not grow — this runs the same step as mk_step with the
+ * same arguments, results and bookkeeping, but every piece of per-step device
+ * scratch the kernel writes comes from one file-scope device array of
+ * 16 MiB that the library holds on each GPU where it is loaded, until the
+ * process exits. The call makes no cudaMalloc, cudaFree or other allocating
+ * call; the context itself must already exist (mk_create allocates).
+ *  - Sizes: a context whose worst-case step scratch exceeds 16 MiB is refused
+ *    with MK_ERR_UNSUPPORTED before any bookkeeping changes (small models
+ *    fit; the 27B-shaped model does not).
+ *  - The first call on a device looks up the array's device address with
+ *    cudaGetSymbolAddress; make that first call before any stream capture.
+ *  - Every call shares the one array and it keeps the previous call's
+ *    contents: the call clears the counters that must start at zero itself.
+ *    Calls whose work overlaps on the GPU (two contexts or two streams at
+ *    once) race on the array and give wrong results; serialise them.
+ */
+mk_status mk_step_static(mk_ctx* ctx, int32_t n_rows, const int32_t* tokens, const int32_t* positions,
+                         const int32_t* seq_ids, const uint8_t* row_flags, int32_t* out_tokens,
+                         int32_t* out_counts);
+
 const char* mk_status_str(mk_status status);
 
 #ifdef __cplusplus

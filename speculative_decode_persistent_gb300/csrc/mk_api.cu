@@ -743,3 +743,122 @@ float mk_last_launch_ms(mk_ctx* c) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Allocation-free step. Everything the persistent kernel writes as per-step
+// scratch (residual and activation rows, split-K partials and their tickets,
+// attention partials and tickets, per-warp argmax records, the result block,
+// the barrier and error words, the staging rows of the attention phase, and
+// the kernel's copy of the model descriptor that points at them) lives in the
+// file-scope array below instead of buffers from cudaMalloc. It is sized once
+// for the life of the process and shared by every call on the same device.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
+__device__ __align__(256) unsigned char g_mk_static_scratch[kStaticScratchBytes];
+constexpr int kMaxDevices = 64;
+void* g_static_addr[kMaxDevices] = {nullptr};
+
+struct StaticLayout {
+  size_t md, x, yin, o, h, partial, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
+      attn_scratch, total;
+};
+
+StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
+  const ModelDesc& md = c->md_host;
+  const size_t nrec = static_cast<size_t>(c->grid) * kWarps;
+  StaticLayout L{};
+  size_t at = 0;
+  auto take = [&](size_t& off, size_t bytes) { off = at; at = align_up(at + (bytes ? bytes : 16)); };
+  take(L.md, sizeof(ModelDesc));
+  take(L.x, static_cast<size_t>(kMaxRows) * md.H * 4);
+  take(L.yin, static_cast<size_t>(kMaxRows) * md.n_in_max * 4);
+  take(L.o, static_cast<size_t>(kMaxRows) * std::max(1, md.o_stride) * 4);
+  take(L.h, static_cast<size_t>(kMaxRows) * md.F * 4);
+  take(L.partial, nrec * md.max_seg * kMaxRows * 32 * 4);
+  take(L.tickets, c->tickets_bytes);
+  take(L.attn_part, static_cast<size_t>(std::max(1, n_attn_items)) * kMaxQRows * (kMaxDh + 2) * 4);
+  take(L.attn_tickets, c->attn_tickets_bytes);
+  take(L.top_val, nrec * kMaxRows * 4);
+  take(L.top_idx, nrec * kMaxRows * 4);
+  take(L.out, kOutInts * 4);
+  take(L.bar, 64);
+  take(L.err, 64);
+  take(L.attn_scratch, nrec * 2 * kMaxDh * 4);
+  L.total = at;
+  return L;
+}
+
+}  // namespace
+
+extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* tokens, const int32_t* positions,
+                                    const int32_t* seq_ids, const uint8_t* row_flags, int32_t* out_tokens,
+                                    int32_t* out_counts) {
+  if (!c) return MK_ERR_INVALID;
+  // The worst case of this context (every attention item a step can have)
+  // must fit, so that the check happens before any bookkeeping changes.
+  const int worst_items = c->grid + kMaxSeqs * std::max(1, c->L.fa_hkv);
+  if (static_layout(c, worst_items).total > kStaticScratchBytes) return MK_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MK_ERR_CUDA;
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mk_static_scratch) != cudaSuccess || !p) return MK_ERR_CUDA;
+    g_static_addr[dev] = p;
+  }
+  mk_status st = mk_step_prepare(c, n_rows, tokens, positions, seq_ids, row_flags);
+  if (st != MK_OK) return st;
+  c->prepared = false;
+  const StaticLayout SL = static_layout(c, c->sd_host->n_attn_items);
+  uint8_t* base = static_cast<uint8_t*>(g_static_addr[dev]);
+  ModelDesc md = c->md_host;
+  md.x = reinterpret_cast<float*>(base + SL.x);
+  md.yin = reinterpret_cast<float*>(base + SL.yin);
+  md.o = reinterpret_cast<float*>(base + SL.o);
+  md.h = reinterpret_cast<float*>(base + SL.h);
+  md.partial = reinterpret_cast<float*>(base + SL.partial);
+  md.tickets = reinterpret_cast<uint32_t*>(base + SL.tickets);
+  md.attn_part = reinterpret_cast<float*>(base + SL.attn_part);
+  md.attn_tickets = reinterpret_cast<uint32_t*>(base + SL.attn_tickets);
+  md.top_val = reinterpret_cast<float*>(base + SL.top_val);
+  md.top_idx = reinterpret_cast<int32_t*>(base + SL.top_idx);
+  md.out = reinterpret_cast<int32_t*>(base + SL.out);
+  md.bar = reinterpret_cast<uint32_t*>(base + SL.bar);
+  md.err = reinterpret_cast<int32_t*>(base + SL.err);
+  ModelDesc* md_dev = reinterpret_cast<ModelDesc*>(base + SL.md);
+  float* attn_scratch = reinterpret_cast<float*>(base + SL.attn_scratch);
+  // The array keeps the previous call's contents: clear what must start at zero.
+  if (cudaMemcpyAsync(md_dev, &md, sizeof(ModelDesc), cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
+      cudaMemsetAsync(md.tickets, 0, c->tickets_bytes, c->stream) != cudaSuccess ||
+      cudaMemsetAsync(md.attn_tickets, 0, c->attn_tickets_bytes, c->stream) != cudaSuccess ||
+      cudaMemsetAsync(md.bar, 0, 64, c->stream) != cudaSuccess ||
+      cudaMemsetAsync(md.err, 0, 64, c->stream) != cudaSuccess ||
+      cudaStreamSynchronize(c->stream) != cudaSuccess)
+    return MK_ERR_CUDA;
+  const cudaError_t e = launch_persistent(md_dev, c->sd_dev, attn_scratch, c->grid, c->stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorCooperativeLaunchTooLarge ? MK_ERR_LAUNCH : MK_ERR_CUDA;
+  }
+  int32_t* h = c->out_host;
+  if (cudaMemcpyAsync(h, md.out, kOutInts * 4, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
+      cudaMemcpyAsync(h + kOutInts, md.err, 16, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
+      cudaStreamSynchronize(c->stream) != cudaSuccess)
+    return MK_ERR_CUDA;
+  if (h[kOutInts] != DEV_OK) return MK_ERR_BARRIER_TIMEOUT;
+  int at = 0;
+  for (int i = 0; i < c->n_seq; ++i) {
+    const int cnt = h[kOutCounts + i];
+    if (cnt < 1 || cnt > c->step_T[i]) return MK_ERR_CUDA;
+    SeqInfo& sq = c->seqs[c->step_seq[i]];
+    sq.pending = true;
+    sq.count = cnt;
+    for (int t = 0; t < c->step_T[i]; ++t) sq.snap_slot[t] = c->step_snap[i][t];
+    if (out_counts) out_counts[i] = cnt;
+    for (int k = 0; k < cnt; ++k) {
+      if (out_tokens) out_tokens[at] = h[kOutTokens + at];
+      ++at;
+    }
+  }
+  return h[kOutInts + 1] ? MK_ERR_NONFINITE : MK_OK;
+}

@@ -91,6 +91,7 @@ def _load():
         "mk_grid_blocks": (i32, [vp]),
         "mk_debug_scratch": (i32, [vp, i32, vp, vp, vp, vp, P(i32), P(i32)]),
         "mk_step_io_bytes": (i32, [vp, P(u64), P(u64)]),
+        "mk_step_static": (i32, [vp, i32, vp, vp, vp, vp, vp, vp]),
         "mk_status_str": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -106,7 +107,7 @@ EXPORTS = ["mk_packed_bytes", "mk_kv_bytes", "mk_kv_scale_bytes", "mk_gdn_state_
            "mk_conv_state_bytes", "mk_create", "mk_free", "mk_seq_set", "mk_seq_reset", "mk_seq_get",
            "mk_step", "mk_step_prepare", "mk_step_launch", "mk_step_finish", "mk_commit",
            "mk_debug_outputs", "mk_last_launch_ms", "mk_debug_skip_arrival", "mk_grid_blocks",
-           "mk_status_str", "mk_debug_scratch", "mk_step_io_bytes"]
+           "mk_status_str", "mk_debug_scratch", "mk_step_io_bytes", "mk_step_static"]
 
 
 def _np_ptr(a):
@@ -275,6 +276,16 @@ class Engine:
         out_c = np.zeros(nseq, np.int32)
         _check(lib.mk_step(self.ctx, len(t), _np_ptr(t), _np_ptr(p), _np_ptr(s), _np_ptr(f), _np_ptr(out_t),
                            _np_ptr(out_c)), "mk_step")
+        return out_t[: int(out_c.sum())], out_c
+
+    def step_static(self, tokens, positions, seq_ids, flags=None):
+        """mk_step_static: the same step with no device allocation."""
+        t, p, s, f = self._rows(tokens, positions, seq_ids, flags)
+        nseq = len({int(x) for x in s})
+        out_t = np.zeros(len(t), np.int32)
+        out_c = np.zeros(nseq, np.int32)
+        _check(lib.mk_step_static(self.ctx, len(t), _np_ptr(t), _np_ptr(p), _np_ptr(s), _np_ptr(f),
+                                  _np_ptr(out_t), _np_ptr(out_c)), "mk_step_static")
         return out_t[: int(out_c.sum())], out_c
 
     def prepare(self, tokens, positions, seq_ids, flags=None):
