@@ -240,6 +240,13 @@ mk_status mk_debug_outputs(mk_ctx* ctx, float* logits, float* hidden);
 mk_status mk_debug_scratch(mk_ctx* ctx, int32_t rows, float* x, float* y, float* o, float* h,
                            int32_t* y_stride, int32_t* o_stride);
 
+/* Test hook: per-phase timeline. When stamps is a device buffer of at least
+ * 5*n_layers + 4 uint64 values, every following launch writes the
+ * %globaltimer value (ns) at its start and when block 0 leaves the grid
+ * barrier closing each phase (embed, then per layer: input GEMM, mixer,
+ * o_proj, gate/up, down; then lm_head; then verify). NULL stops it. */
+mk_status mk_debug_timeline(mk_ctx* ctx, uint64_t* stamps);
+
 /* Device-side timing of the last mk_step_launch in milliseconds (CUDA events
  * on the context stream); negative if unavailable. */
 float mk_last_launch_ms(mk_ctx* ctx);

@@ -129,10 +129,10 @@ int max_segments(int n_tiles, int nsb, int grid) {
     const Sched sc = make_sched(nsb, R);
     for (int sl = 0; sl < sc.S; ++sl) {
       const int nsb_s = slice_nsb(sc, nsb, sl);
-      const int64_t Us = static_cast<int64_t>(n_tiles) * nsb_s;
-      const int64_t Ws = static_cast<int64_t>(slice_cta0(sc, grid, sl + 1) - slice_cta0(sc, grid, sl)) * kWarps;
-      for (int64_t ws = 0; ws < Ws; ++ws) {
-        const int64_t u0 = warp_u0(Us, Ws, ws), u1 = warp_u0(Us, Ws, ws + 1);
+      const uint32_t Us = static_cast<uint32_t>(n_tiles) * nsb_s;
+      const uint32_t Ws = static_cast<uint32_t>(slice_cta0(sc, grid, sl + 1) - slice_cta0(sc, grid, sl)) * kWarps;
+      for (uint32_t ws = 0; ws < Ws; ++ws) {
+        const uint32_t u0 = warp_u0(Us, Ws, ws), u1 = warp_u0(Us, Ws, ws + 1);
         if (u1 > u0) best = std::max(best, static_cast<int>((u1 - 1) / nsb_s - u0 / nsb_s + 1));
       }
     }
@@ -193,8 +193,6 @@ cudaError_t dev_alloc(mk_ctx* c, T** p, size_t bytes) {
   *p = static_cast<T*>(v);
   return cudaMemsetAsync(v, 0, bytes ? bytes : 16, c->stream);
 }
-
-mk_status fail_cuda() { return MK_ERR_CUDA; }
 
 void release_pages(mk_ctx* c, SeqInfo& s) {
   const int need = (s.len + c->L.page_tokens - 1) / c->L.page_tokens;
@@ -417,6 +415,7 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   c->tickets_bytes = static_cast<size_t>(max_tiles) * 4;
   c->attn_tickets_bytes = static_cast<size_t>(kMaxSeqs) * std::max(1, L.fa_hkv) * 4;
   if ((e = dev_alloc(c, &md.x, static_cast<size_t>(kMaxRows) * H * 4)) ||
+      (e = dev_alloc(c, &md.xsq, static_cast<size_t>(H / 32) * kMaxRows * 4)) ||
       (e = dev_alloc(c, &md.yin, static_cast<size_t>(kMaxRows) * p.n_in_max * 4)) ||
       (e = dev_alloc(c, &md.o, static_cast<size_t>(kMaxRows) * std::max(1, p.o_stride) * 4)) ||
       (e = dev_alloc(c, &md.h, static_cast<size_t>(kMaxRows) * F * 4)) ||
@@ -510,6 +509,15 @@ mk_status mk_debug_outputs(mk_ctx* c, float* logits, float* hidden) {
   if (!c) return MK_ERR_INVALID;
   c->md_host.dbg_logits = logits;
   c->md_host.dbg_hidden = hidden;
+  if (cudaMemcpyAsync(c->md_dev, &c->md_host, sizeof(ModelDesc), cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
+      cudaStreamSynchronize(c->stream) != cudaSuccess)
+    return MK_ERR_CUDA;
+  return MK_OK;
+}
+
+mk_status mk_debug_timeline(mk_ctx* c, uint64_t* stamps) {
+  if (!c) return MK_ERR_INVALID;
+  c->md_host.dbg_time = stamps;
   if (cudaMemcpyAsync(c->md_dev, &c->md_host, sizeof(ModelDesc), cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
       cudaStreamSynchronize(c->stream) != cudaSuccess)
     return MK_ERR_CUDA;
@@ -625,7 +633,9 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
   int total_tiles = 0;
   for (int i = 0; i < n_seq; ++i) total_tiles += (c->seqs[sid[i]].len + 31) / 32;
   const int hkv = std::max(1, L.fa_hkv);
-  const int tps = std::max(1, (total_tiles * hkv + c->grid - 1) / c->grid);
+  int tps = std::max(1, (total_tiles * hkv + c->grid - 1) / c->grid);
+  for (int i = 0; i < n_seq; ++i)  // at most kMaxSplits parts per (sequence, kv head)
+    tps = std::max(tps, ((c->seqs[sid[i]].len + 31) / 32 + kMaxSplits - 1) / kMaxSplits);
   int items = 0;
   for (int i = 0; i < n_seq; ++i) {
     const SeqInfo& s = c->seqs[sid[i]];
@@ -760,7 +770,7 @@ constexpr int kMaxDevices = 64;
 void* g_static_addr[kMaxDevices] = {nullptr};
 
 struct StaticLayout {
-  size_t md, x, yin, o, h, partial, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
+  size_t md, x, xsq, yin, o, h, partial, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
       attn_scratch, total;
 };
 
@@ -772,6 +782,7 @@ StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
   auto take = [&](size_t& off, size_t bytes) { off = at; at = align_up(at + (bytes ? bytes : 16)); };
   take(L.md, sizeof(ModelDesc));
   take(L.x, static_cast<size_t>(kMaxRows) * md.H * 4);
+  take(L.xsq, static_cast<size_t>(md.H / 32) * kMaxRows * 4);
   take(L.yin, static_cast<size_t>(kMaxRows) * md.n_in_max * 4);
   take(L.o, static_cast<size_t>(kMaxRows) * std::max(1, md.o_stride) * 4);
   take(L.h, static_cast<size_t>(kMaxRows) * md.F * 4);
@@ -813,6 +824,7 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
   uint8_t* base = static_cast<uint8_t*>(g_static_addr[dev]);
   ModelDesc md = c->md_host;
   md.x = reinterpret_cast<float*>(base + SL.x);
+  md.xsq = reinterpret_cast<float*>(base + SL.xsq);
   md.yin = reinterpret_cast<float*>(base + SL.yin);
   md.o = reinterpret_cast<float*>(base + SL.o);
   md.h = reinterpret_cast<float*>(base + SL.h);

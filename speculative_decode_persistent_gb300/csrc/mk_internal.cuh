@@ -11,8 +11,9 @@
 namespace mk {
 
 // ------------------------------------------------------------------ launch
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 8;                      // math warps
+constexpr int kThreads = kWarps * 32;           // math threads (named barrier 1)
+constexpr int kLaunchThreads = kThreads + 32;   // + one producer warp streaming weights
 
 // ------------------------------------------------------------- Q4 "units"
 // The GEMM phases stream weights as units of 32 output rows x 256 k
@@ -26,29 +27,28 @@ constexpr int kUnitHdr = 512;
 constexpr int kTileRows = 32;
 
 // Per-warp ring of streamed units (bulk async copies, mbarrier completion).
-constexpr int kRing = 3;
+constexpr int kRing = 4;
 
 // ----------------------------------------------------------- shared memory
-constexpr int kRingBytes = kWarps * kRing * kUnitBytes;   // 110592
-constexpr int kScaleTab = 2048;                           // [j8][g8][rb2][4 x u32]
-constexpr int kDTab = 128;                                // [g8][rb2][hi2] fp32
-constexpr int kWarpTab = kScaleTab + kDTab;               // 2176
-constexpr int kTabBytes = kWarps * kWarpTab;              // 17408
-constexpr int kActBytes = 96 * 1024;                      // activations / phase scratch
+constexpr int kRingBytes = kWarps * kRing * kUnitBytes;   // 147456
+constexpr int kScaleTab = 2048;  // [j8][g8][rb2][hi2] fp32 scales (1 KB); 2 KB as the flush stage
+constexpr int kWarpTab = kScaleTab + 128;                 // 2176 per buffer
+constexpr int kTabBytes = kWarps * 2 * kWarpTab;          // 34816 (double-buffered per warp)
+constexpr int kActBytes = 44 * 1024;                      // activations / phase scratch
 constexpr int kMiscBytes = 4096;
-constexpr int kBarBytes = kWarps * kRing * 8;
+constexpr int kBarBytes = 2 * kWarps * kRing * 8;  // full + empty barriers
 
 constexpr int kOffRing = 0;
 constexpr int kOffTab = kOffRing + kRingBytes;
 constexpr int kOffAct = kOffTab + kTabBytes;
 constexpr int kOffMisc = kOffAct + kActBytes;
 constexpr int kOffBar = kOffMisc + kMiscBytes;
-constexpr int kSmemBytes = kOffBar + kBarBytes;           // 229568
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
+constexpr int kSmemBytes = kOffBar + kBarBytes;           // 231936
+static_assert(kSmemBytes + 256 <= 232448, "exceeds the 227 KB per-block limit");
 // Attention and Gated DeltaNet phases may use the table and activation
 // regions together (they never hold a GEMM's data at that time).
 constexpr int kOffPhase = kOffTab;
-constexpr int kPhaseBytes = kTabBytes + kActBytes;        // 115712
+constexpr int kPhaseBytes = kTabBytes + kActBytes;        // 79872
 
 // --------------------------------------------------------------- limits
 constexpr int kMaxRows = MK_MAX_DECODE_ROWS;  // 12: at most 3 column tiles of 8
@@ -56,6 +56,7 @@ constexpr int kMaxT = MK_MAX_T;
 constexpr int kMaxSeqs = MK_MAX_SEQS;
 constexpr int kMaxDh = 256;
 constexpr int kMaxQRows = 48;                 // T x (hq/hkv) rows attending one kv head
+constexpr int kMaxSplits = 128;               // split-K parts of one (sequence, kv head)
 
 // ------------------------------------------------------------- descriptors
 enum Prologue : int32_t { PRO_RMS_X = 0, PRO_GDN_OUT = 1, PRO_FA_OUT = 2, PRO_H = 3 };
@@ -91,6 +92,7 @@ struct ModelDesc {
   float* gdn_state; float* conv_state;
   // scratch
   float* x;          // [kMaxRows][H] residual stream
+  float* xsq;        // [H/32][kMaxRows] sums of squares of x over each 32-wide chunk
   float* yin;        // [kMaxRows][n_in_max] input projections
   float* o;          // [kMaxRows][o_stride] mixer outputs
   float* h;          // [kMaxRows][F] SwiGLU outputs
@@ -106,6 +108,7 @@ struct ModelDesc {
   int32_t* err;      // [0] error code, [1] non-finite flag, [2] detail
   float* dbg_logits; // optional
   float* dbg_hidden; // optional
+  uint64_t* dbg_time;  // optional: [phases + 1] %globaltimer stamps by block 0
 };
 
 // Device result block layout.
@@ -153,13 +156,15 @@ struct Sched {
 __host__ __device__ inline int act_col_stride(int nsb_slice) { return nsb_slice * 512 + 64; }
 
 __host__ __device__ inline int act_bytes(int nsb_slice, int R) {
-  return 2 * R * act_col_stride(nsb_slice) + nsb_slice * 8 * R * 4;
+  return 2 * R * act_col_stride(nsb_slice) + nsb_slice * 8 * R * 4;  // = 1056 R n + 128 R
 }
 
 __host__ __device__ inline Sched make_sched(int nsb, int R) {
+  // largest slice with act_bytes(n, R) = 1056 R n + 128 R <= kActBytes
   Sched s;
-  int max_sb = 1;
-  while (max_sb < nsb && act_bytes(max_sb + 1, R) <= kActBytes) ++max_sb;
+  int max_sb = (kActBytes - 128 * R) / (1056 * R);
+  if (max_sb < 1) max_sb = 1;
+  if (max_sb > nsb) max_sb = nsb;
   s.S = (nsb + max_sb - 1) / max_sb;
   s.sb_per = (nsb + s.S - 1) / s.S;
   return s;
@@ -172,20 +177,27 @@ __host__ __device__ inline int slice_nsb(const Sched& s, int nsb, int sl) {
   return e - b;
 }
 __host__ __device__ inline int slice_cta0(const Sched& s, int grid, int sl) {
-  return (int)((int64_t)sl * grid / s.S);
+  return static_cast<int>(static_cast<uint32_t>(sl) * grid / s.S);
 }
 __host__ __device__ inline int slice_of_cta(const Sched& s, int grid, int cta) {
   // largest sl with slice_cta0(sl) <= cta
-  int sl = (int)(((int64_t)(cta + 1) * s.S - 1) / grid);
-  return sl;
+  return static_cast<int>((static_cast<uint32_t>(cta + 1) * s.S - 1) / grid);
 }
-// Units [u0, u1) of slice-local warp ws out of Ws warps over Us units.
-__host__ __device__ inline int64_t warp_u0(int64_t Us, int64_t Ws, int64_t ws) {
+// Units [u0, u1) of slice-local warp ws out of Ws warps over Us units
+// (32-bit: units x warps stays far below 2^32 for every supported shape).
+__host__ __device__ inline uint32_t warp_u0(uint32_t Us, uint32_t Ws, uint32_t ws) {
   return ws * Us / Ws;
 }
 // Slice-local warp whose range holds unit u.
-__host__ __device__ inline int64_t warp_of_unit(int64_t Us, int64_t Ws, int64_t u) {
+__host__ __device__ inline uint32_t warp_of_unit(uint32_t Us, uint32_t Ws, uint32_t u) {
   return ((u + 1) * Ws - 1) / Us;
+}
+// Number of warp ranges that hold units [a, b) of a slice. The even split
+// gives every warp floor or ceil(Us/Ws) units: with Us < Ws a range holds at
+// most one unit, otherwise none is empty.
+__host__ __device__ inline uint32_t segments_in(uint32_t Us, uint32_t Ws, uint32_t a, uint32_t b) {
+  if (Us < Ws) return b - a;
+  return warp_of_unit(Us, Ws, b - 1) - warp_of_unit(Us, Ws, a) + 1;
 }
 
 }  // namespace mk

@@ -17,12 +17,13 @@
 // streaming weights while the barrier settles.
 //
 // Skinny GEMM arithmetic (all rows of the step against each weight once):
-// 4-bit codes become exact fp16 integers sc_j*q with one lop3 and one fused
-// multiply-add per pair; the activations are split into two fp16 parts
-// (high + low) so that the m16n8k16 products stay exact to ~2^-22; each
-// super-block's fp16 tile sums are scaled by d in fp32 and the min term
-// dmin * sum_j m_j * sum(x over sub-block j) is added by the lane that owns
-// the weight row. Weights are therefore used exactly as stored.
+// a 4-bit code masked into the low mantissa bits of an fp16 is the exact
+// subnormal q * 2^-24 (or q * 2^-20 for the nibble 4 bits up), so one AND per
+// pair of weights feeds m16n8k16 directly; the activations are split into two
+// fp16 parts (high + low) so that the products stay exact to ~2^-22; each
+// 32-wide sub-block's two mma sums are scaled in fp32 by d * sc_j * 2^24 (or
+// 2^20), and the min term dmin * sum_j m_j * sum(x over sub-block j) is added
+// by the lane that owns the weight row. Weights are used exactly as stored.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -89,11 +90,6 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint3
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(magic));
   return r;
 }
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -118,6 +114,11 @@ __device__ __forceinline__ void ldsm_x2_trans(uint32_t& r0, uint32_t& r1, const 
                : "=r"(r0), "=r"(r1)
                : "r"(smem_u32(p)));
 }
+// Barrier among the math warps only (the producer warp never joins it).
+__device__ __forceinline__ void math_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -139,14 +140,14 @@ struct Smem {
   __device__ uint8_t* ring(int warp, int slot) const {
     return base + kOffRing + (warp * kRing + slot) * kUnitBytes;
   }
-  __device__ uint64_t* bar(int warp, int slot) const {
+  __device__ uint64_t* bar(int warp, int slot) const {  // full: the unit has landed
     return reinterpret_cast<uint64_t*>(base + kOffBar) + warp * kRing + slot;
   }
-  __device__ uint32_t* stab(int warp) const {
-    return reinterpret_cast<uint32_t*>(base + kOffTab + warp * kWarpTab);
+  __device__ uint64_t* empty(int warp, int slot) const {  // the math warp is done with the slot
+    return reinterpret_cast<uint64_t*>(base + kOffBar) + kWarps * kRing + warp * kRing + slot;
   }
-  __device__ float* dtab(int warp) const {
-    return reinterpret_cast<float*>(base + kOffTab + warp * kWarpTab + kScaleTab);
+  __device__ uint32_t* stab(int warp, int buf) const {
+    return reinterpret_cast<uint32_t*>(base + kOffTab + (warp * 2 + buf) * kWarpTab);
   }
   __device__ uint8_t* act() const { return base + kOffAct; }
   __device__ float* misc() const { return reinterpret_cast<float*>(base + kOffMisc); }
@@ -154,57 +155,54 @@ struct Smem {
 };
 
 // -------------------------------------------------------------- grid sync
-// Sense by generation: read the generation, arrive, and wait (bounded) until
-// the last arriver bumps it. An error word set by any block makes every
-// waiter leave at its next check; a wait that outlives the deadline sets it.
+// A monotonic arrival counter (zeroed before each launch): barrier n is
+// complete when the counter reaches (n+1) * gridDim.x. Arrival is a release
+// reduction (no round trip); thread 0 of each block polls with acquire loads.
+// An error word set by any block makes every waiter leave; a wait that
+// outlives the deadline sets it.
 __device__ bool grid_sync(const ModelDesc& md, const StepDesc& sd, int& nbar, int* sflag) {
-  __syncthreads();
+  math_sync();
   if (threadIdx.x == 0) {
     int ok = 1;
     volatile int32_t* err = md.err;
-    const uint32_t gen = ld_acquire(&md.bar[1]);
+    const uint32_t target = static_cast<uint32_t>(nbar + 1) * gridDim.x;
     const bool skip = sd.skip_block == static_cast<int>(blockIdx.x) && sd.skip_barrier == nbar;
-    if (*err == 0 && !skip) {
+    if (!skip) {
       __threadfence();
-      const uint32_t arrived = atomicAdd(&md.bar[0], 1u) + 1u;
-      if (arrived == gridDim.x) {
-        atomicExch(&md.bar[0], 0u);
-        __threadfence();
-        st_release(&md.bar[1], gen + 1u);
-      }
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(md.bar) : "memory");
     }
-    const uint64_t t0 = globaltimer();
-    uint32_t ns = 32;
+    uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-      if (ld_acquire(&md.bar[1]) != gen) break;
-      if (*err != 0) { ok = 0; break; }
-      if (globaltimer() - t0 > sd.barrier_timeout_ns || it > (1u << 28)) {
-        atomicCAS(md.err, 0, DEV_BARRIER_TIMEOUT);
-        ok = 0;
-        break;
+      if (ld_acquire(md.bar) >= target) break;
+      if ((it & 31u) == 31u) {
+        if (*err != 0) { ok = 0; break; }
+        const uint64_t now = globaltimer();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > sd.barrier_timeout_ns || it > (1u << 30)) {
+          atomicCAS(md.err, 0, DEV_BARRIER_TIMEOUT);
+          ok = 0;
+          break;
+        }
       }
-      __nanosleep(ns);
-      if (ns < 256) ns <<= 1;
     }
     if (*err != 0) ok = 0;
-    __threadfence();
     *sflag = ok;
   }
-  __syncthreads();
+  math_sync();
   ++nbar;
   return *sflag != 0;
 }
 
 // ------------------------------------------------------------ the stream
+// The producer warp feeds every math warp's ring: lane w (< kWarps) walks math
+// warp w's unit sequence over all GEMM phases of the step (the schedule is
+// static) and issues one bulk copy per unit as soon as the slot it goes to is
+// free, so copies run ahead across grid barriers and mixer phases. Math warps
+// wait on the slot's "full" barrier and release it through its "empty" one.
 struct WarpCtx {
   int warp, lane, gid;
-  uint32_t c_pos, p_pos;
-  int p_gp;
-  bool p_done;
-  int64_t p_u, p_u1;
-  int p_nsb_s, p_sb0, p_nsb;
-  const uint8_t* p_w;
-  uint64_t pol;
+  uint32_t c_pos;  // units consumed by this math warp
 };
 
 __device__ __forceinline__ const GemmDesc& gemm_desc(const ModelDesc& md, int gp) {
@@ -217,7 +215,7 @@ __device__ __forceinline__ const GemmDesc& gemm_desc(const ModelDesc& md, int gp
 struct Assign {
   Sched sc;
   int sl, nsb_s, sb0, cta0;
-  int64_t Us, Ws, ws, u0, u1;
+  uint32_t Us, Ws, ws, u0, u1;
 };
 
 __device__ __forceinline__ Assign assign_for(const GemmDesc& g, int R, int grid, int cta, int warp) {
@@ -228,65 +226,114 @@ __device__ __forceinline__ Assign assign_for(const GemmDesc& g, int R, int grid,
   const int cta1 = slice_cta0(a.sc, grid, a.sl + 1);
   a.nsb_s = slice_nsb(a.sc, g.nsb, a.sl);
   a.sb0 = slice_sb0(a.sc, a.sl);
-  a.Us = static_cast<int64_t>(g.n_tiles) * a.nsb_s;
-  a.Ws = static_cast<int64_t>(cta1 - a.cta0) * kWarps;
-  a.ws = static_cast<int64_t>(cta - a.cta0) * kWarps + warp;
+  a.Us = static_cast<uint32_t>(g.n_tiles) * a.nsb_s;
+  a.Ws = static_cast<uint32_t>(cta1 - a.cta0) * kWarps;
+  a.ws = static_cast<uint32_t>(cta - a.cta0) * kWarps + warp;
   a.u0 = warp_u0(a.Us, a.Ws, a.ws);
   a.u1 = warp_u0(a.Us, a.Ws, a.ws + 1);
   return a;
 }
 
-// Issue the bulk copies of this warp's next units until its ring is full.
-__device__ void produce(WarpCtx& wc, const ModelDesc& md, const StepDesc& sd, const Smem& sm) {
-  while (!wc.p_done && wc.p_pos - wc.c_pos < static_cast<uint32_t>(kRing)) {
-    if (wc.p_u >= wc.p_u1) {
-      ++wc.p_gp;
-      if (wc.p_gp > 4 * md.n_layers) { wc.p_done = true; break; }
-      const GemmDesc& g = gemm_desc(md, wc.p_gp);
-      const Assign a = assign_for(g, sd.R, gridDim.x, blockIdx.x, wc.warp);
-      wc.p_u = a.u0;
-      wc.p_u1 = a.u1;
-      wc.p_nsb_s = a.nsb_s;
-      wc.p_sb0 = a.sb0;
-      wc.p_nsb = g.nsb;
-      wc.p_w = g.w;
-      continue;
-    }
-    const int slot = wc.p_pos % kRing;
-    if (wc.lane == 0) {
-      const int64_t tile = wc.p_u / wc.p_nsb_s;
-      const int sb = wc.p_sb0 + static_cast<int>(wc.p_u % wc.p_nsb_s);
-      const uint8_t* src = wc.p_w + (static_cast<size_t>(tile) * wc.p_nsb + sb) * kUnitBytes;
-      uint64_t* b = sm.bar(wc.warp, slot);
-      mbar_arrive_expect_tx(b, kUnitBytes);
-      bulk_g2s(sm.ring(wc.warp, slot), src, kUnitBytes, b, wc.pol);
-    }
-    ++wc.p_u;
-    ++wc.p_pos;
-  }
-}
-
-__device__ bool wait_unit(const WarpCtx& wc, const Smem& sm, const ModelDesc& md, uint64_t timeout_ns) {
-  const int slot = wc.c_pos % kRing;
-  const uint32_t parity = (wc.c_pos / kRing) & 1u;
-  uint64_t* b = sm.bar(wc.warp, slot);
+// Bounded wait for an mbarrier phase; false (and the error word set) on timeout
+// or when another block has already reported an error.
+__device__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity, const ModelDesc& md, uint64_t timeout_ns,
+                                  int32_t code) {
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = globaltimer();
+  volatile int32_t* err = md.err;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(b, parity)) return true;
+    if ((it & 63u) == 0 && *err != 0) return false;
     if (globaltimer() - t0 > timeout_ns || it > (1u << 26)) {
-      atomicCAS(md.err, 0, DEV_COPY_TIMEOUT);
+      atomicCAS(md.err, 0, code);
       return false;
     }
   }
 }
 
-// Wait (bounded) for every copy this warp still has in flight.
-__device__ void drain(WarpCtx& wc, const Smem& sm, const ModelDesc& md) {
-  while (wc.c_pos < wc.p_pos) {
-    wait_unit(wc, sm, md, 50000000ull);
-    ++wc.c_pos;
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Lanes 0..kWarps-1 each walk one math warp's unit sequence; the warp stays
+// converged: every sweep, each lane issues its next unit if that unit's slot
+// has been released, then the sweep repeats until every lane is done.
+__device__ void producer_warp(const ModelDesc& md, const StepDesc& sd, const Smem& sm) {
+  const int lane = threadIdx.x & 31;
+  const int w = lane < kWarps ? lane : 0;
+  const uint64_t pol = evict_first_policy();
+  int gp = -1;
+  uint32_t left = 0, tile = 0, sbl = 0, p = 0;
+  int nsb_s = 1, sb0 = 0, nsb = 1;
+  const uint8_t* wsrc = nullptr;
+  bool done = lane >= kWarps;
+  volatile int32_t* err = md.err;
+  uint64_t t_idle = 0;
+  for (uint32_t sweep = 0;; ++sweep) {
+    // advance to the next phase with units for this lane's warp
+    while (!done && left == 0) {
+      if (++gp > 4 * md.n_layers) { done = true; break; }
+      const GemmDesc& g = gemm_desc(md, gp);
+      const Assign a = assign_for(g, sd.R, gridDim.x, blockIdx.x, w);
+      left = a.u1 - a.u0;
+      nsb_s = a.nsb_s;
+      tile = a.u0 / nsb_s;
+      sbl = a.u0 - tile * nsb_s;
+      sb0 = a.sb0;
+      nsb = g.nsb;
+      wsrc = g.w;
+    }
+    if (__all_sync(0xffffffffu, done)) break;
+    bool issued = false;
+    if (!done) {
+      const int slot = p % kRing;
+      if (mbar_test(sm.empty(w, slot), ((p / kRing) & 1u) ^ 1u)) {
+        uint64_t* b = sm.bar(w, slot);
+        mbar_arrive_expect_tx(b, kUnitBytes);
+        bulk_g2s(sm.ring(w, slot), wsrc + (static_cast<size_t>(tile) * nsb + sb0 + sbl) * kUnitBytes, kUnitBytes,
+                 b, pol);
+        if (++sbl == static_cast<uint32_t>(nsb_s)) { sbl = 0; ++tile; }
+        --left;
+        ++p;
+        issued = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, issued)) {
+      t_idle = 0;
+    } else if ((sweep & 63u) == 63u) {
+      // nothing could be issued: the math warps are behind; give up only on
+      // an error or after the deadline
+      if (*err != 0) break;
+      const uint64_t now = globaltimer();
+      if (t_idle == 0) t_idle = now;
+      else if (now - t_idle > sd.barrier_timeout_ns) { atomicCAS(md.err, 0, DEV_COPY_TIMEOUT); break; }
+    }
   }
+  // the block must not exit while a copy into its shared memory is in flight
+  if (lane < kWarps)
+    for (uint32_t q = p > static_cast<uint32_t>(kRing) ? p - kRing : 0; q < p; ++q)
+      mbar_wait_bounded(sm.bar(w, q % kRing), (q / kRing) & 1u, md, 50000000ull, DEV_COPY_TIMEOUT);
+}
+
+__device__ __forceinline__ bool wait_unit(const WarpCtx& wc, const Smem& sm, const ModelDesc& md,
+                                          uint64_t timeout_ns) {
+  return mbar_wait_bounded(sm.bar(wc.warp, wc.c_pos % kRing), (wc.c_pos / kRing) & 1u, md, timeout_ns,
+                           DEV_COPY_TIMEOUT);
+}
+
+// The math warp is done reading its current slot.
+__device__ __forceinline__ void release_unit(WarpCtx& wc, const Smem& sm) {
+  __syncwarp();
+  if (wc.lane == 0) mbar_arrive(sm.empty(wc.warp, wc.c_pos % kRing));
+  ++wc.c_pos;
 }
 
 // ------------------------------------------------------------------ embed
@@ -306,13 +353,20 @@ __device__ void embed_phase(const ModelDesc& md, const StepDesc& sd, const WarpC
     const float sc = static_cast<float>((lo64 >> (6 * j)) & 63u);
     const float m = static_cast<float>((mid64 >> (16 + 6 * j)) & 63u);
     const float ds = d * sc, dm = dmin * m;
+    float sq = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int i = i0 + e;
       const uint8_t byte = __ldg(blk + 16 + 16 * j + (i % 16));
       const int q = i < 16 ? (byte & 15) : (byte >> 4);
-      md.x[static_cast<size_t>(r) * md.H + sb * 256 + 32 * j + i] = ds * static_cast<float>(q) - dm;
+      const float xv = ds * static_cast<float>(q) - dm;
+      md.x[static_cast<size_t>(r) * md.H + sb * 256 + 32 * j + i] = xv;
+      sq = fmaf(xv, xv, sq);
     }
+    // the 4 lanes of sub-block j hold one 32-wide chunk
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+    if ((wc.lane & 3) == 0) md.xsq[static_cast<size_t>(sb * 8 + j) * kMaxRows + r] = sq;
   }
 }
 
@@ -320,7 +374,8 @@ __device__ void embed_phase(const ModelDesc& md, const StepDesc& sd, const WarpC
 // Fills the activation region for reduction slice [sb0, sb0 + nsb_s): for each
 // row r, column 2r holds the fp16 high part and column 2r+1 the low part of the
 // input vector, each column in the per-32 permuted order of the B fragments;
-// then sx[sb][j][r] = sum of (high + low) over sub-block j.
+// then sx[sb][j][r] = sum of (high + low) over sub-block j. Loads are float4,
+// and per-row norms reduce over the whole block in a fixed order.
 __device__ __forceinline__ int act_perm(int kl) {
   const int i = kl & 31;
   const int ks_in = i >> 4, rr = i & 15;
@@ -328,88 +383,124 @@ __device__ __forceinline__ int act_perm(int kl) {
   return (kl & ~31) + c * 8 + ks_in * 4 + half * 2 + e;
 }
 
+__device__ __forceinline__ void put_act(__half* act, int cs2, int R, float* sx, int r, int kl, const float (&u)[4],
+                                        int lane) {
+  __half hi[4], lo[4];
+  float part = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    hi[e] = __float2half_rn(u[e]);
+    lo[e] = __float2half_rn(u[e] - __half2float(hi[e]));
+    part += __half2float(hi[e]) + __half2float(lo[e]);
+  }
+  // k and k+1 (and k+2, k+3) are adjacent pairs in the permuted order
+  const int p0 = act_perm(kl), p2 = act_perm(kl + 2);
+  __half* chi = act + (2 * r) * cs2;
+  __half* clo = act + (2 * r + 1) * cs2;
+  *reinterpret_cast<__half2*>(chi + p0) = __halves2half2(hi[0], hi[1]);
+  *reinterpret_cast<__half2*>(chi + p2) = __halves2half2(hi[2], hi[3]);
+  *reinterpret_cast<__half2*>(clo + p0) = __halves2half2(lo[0], lo[1]);
+  *reinterpret_cast<__half2*>(clo + p2) = __halves2half2(lo[2], lo[3]);
+  // 8 consecutive threads hold one 32-wide sub-block
+  part += __shfl_xor_sync(0xffffffffu, part, 1);
+  part += __shfl_xor_sync(0xffffffffu, part, 2);
+  part += __shfl_xor_sync(0xffffffffu, part, 4);
+  if ((lane & 7) == 0) sx[((kl >> 8) * 8 + ((kl & 255) >> 5)) * R + r] = part;
+}
+
+// One round of loads: every thread issues all of its source float4 loads
+// (up to kB groups, plus the per-chunk sums of squares for an RMSNorm) before
+// using any of them, so the prologue costs about one L2 round trip.
+// RMSNorm: 1/rms from the 32-wide chunk sums the residual writers left, added
+// in a fixed order. Gated DeltaNet output: each head's 128 (or 64) values are
+// the float4s of 32 (or 16) consecutive lanes, so its norm is a shuffle sum.
 __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g, int sb0,
                               int nsb_s, const Smem& sm) {
+  constexpr int kB = 8;
   const int R = sd.R;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = sb0 * 256, ks = nsb_s * 256;
   const int cstride = act_col_stride(nsb_s);
   __half* act = reinterpret_cast<__half*>(sm.act());
   float* sx = reinterpret_cast<float*>(sm.act() + 2 * R * cstride);
-  float* misc = sm.misc();
-  if (g.pro == PRO_RMS_X) {
-    for (int r = warp; r < R; r += kWarps) {
-      const float* x = md.x + static_cast<size_t>(r) * md.H;
-      float ss = 0.f;
-      for (int k = lane; k < md.H; k += 32) {
-        const float v = __ldcg(x + k);
-        ss = fmaf(v, v, ss);
+  float* misc = sm.misc();                        // 1/rms per row
+  float* red = misc + 1024 - kWarps * kMaxRows;   // [warp][row] partial sums
+  const int per_row = ks / 4;
+  const int cs2 = cstride / 2;
+  const int total = R * per_row;
+  const int nchunk = md.H / 32;
+  for (int base = 0; base < total; base += kThreads * kB) {
+    float4 s1[kB], s2[kB];
+    float sq[kMaxRows];
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int idx = base + b * kThreads + tid;
+      s1[b] = s2[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (idx < total) {
+        const int r = idx / per_row, k = k0 + (idx - r * per_row) * 4;
+        if (g.pro == PRO_RMS_X) {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.x + static_cast<size_t>(r) * md.H + k));
+        } else if (g.pro == PRO_GDN_OUT) {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
+          s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.conv_ch + k));
+        } else if (g.pro == PRO_FA_OUT) {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
+          s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.hq * md.dh + k));
+        } else {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.h + static_cast<size_t>(r) * md.F + k));
+        }
       }
-      ss = warp_sum(ss);
-      if (lane == 0) misc[r] = 1.0f / sqrtf(ss / static_cast<float>(md.H) + md.eps);
     }
-  } else if (g.pro == PRO_GDN_OUT) {
-    const int h0 = k0 / md.dv, nh = ks / md.dv;
-    for (int p = warp; p < R * nh; p += kWarps) {
-      const int r = p / nh, hh = h0 + p % nh;
-      const float* o = md.o + static_cast<size_t>(r) * md.o_stride + hh * md.dv;
-      float ss = 0.f;
-      for (int i = lane; i < md.dv; i += 32) {
-        const float v = __ldcg(o + i);
-        ss = fmaf(v, v, ss);
+    if (g.pro == PRO_RMS_X && base == 0) {
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        sq[r] = 0.f;
+        if (r < R)
+          for (int c = tid; c < nchunk; c += kThreads) sq[r] += __ldcg(md.xsq + static_cast<size_t>(c) * kMaxRows + r);
       }
-      ss = warp_sum(ss);
-      if (lane == 0) misc[p] = 1.0f / sqrtf(ss / static_cast<float>(md.dv) + md.eps);
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r)
+        if (r < R) {
+          const float t = warp_sum(sq[r]);
+          if (lane == 0) red[warp * kMaxRows + r] = t;
+        }
+      math_sync();
+      if (tid < R) {
+        float t = 0.f;
+        for (int w = 0; w < kWarps; ++w) t += red[w * kMaxRows + tid];
+        misc[tid] = 1.0f / sqrtf(t / static_cast<float>(md.H) + md.eps);
+      }
+      math_sync();
+    }
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int idx = base + b * kThreads + tid;
+      if (idx < total) {  // warp-uniform: total is a multiple of 64
+        const int r = idx / per_row, kl = (idx - r * per_row) * 4, k = k0 + kl;
+        float u[4];
+        if (g.pro == PRO_RMS_X) {
+          const float4 gg = *reinterpret_cast<const float4*>(g.gain + k);
+          const float sc = misc[r];
+          u[0] = s1[b].x * sc * gg.x; u[1] = s1[b].y * sc * gg.y; u[2] = s1[b].z * sc * gg.z; u[3] = s1[b].w * sc * gg.w;
+        } else if (g.pro == PRO_GDN_OUT) {
+          float hs = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, s1[b].w * s1[b].w)));
+          for (int off = 1; off < md.dv / 4; off <<= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
+          const float sc = 1.0f / sqrtf(hs / static_cast<float>(md.dv) + md.eps);
+          const int i = k % md.dv;
+          const float4 gg = *reinterpret_cast<const float4*>(g.gain + i);
+          u[0] = s1[b].x * sc * gg.x * siluf_(s2[b].x); u[1] = s1[b].y * sc * gg.y * siluf_(s2[b].y);
+          u[2] = s1[b].z * sc * gg.z * siluf_(s2[b].z); u[3] = s1[b].w * sc * gg.w * siluf_(s2[b].w);
+        } else if (g.pro == PRO_FA_OUT) {
+          u[0] = s1[b].x * sigmoidf_(s2[b].x); u[1] = s1[b].y * sigmoidf_(s2[b].y);
+          u[2] = s1[b].z * sigmoidf_(s2[b].z); u[3] = s1[b].w * sigmoidf_(s2[b].w);
+        } else {
+          u[0] = s1[b].x; u[1] = s1[b].y; u[2] = s1[b].z; u[3] = s1[b].w;
+        }
+        put_act(act, cs2, R, sx, r, kl, u, lane);
+      }
     }
   }
-  __syncthreads();
-  const int total = R * ks;
-  const int h0 = k0 / (md.dv > 0 ? md.dv : 1), nh = ks / (md.dv > 0 ? md.dv : 1);
-  for (int idx = tid; idx < total; idx += kThreads) {
-    const int r = idx / ks, kl = idx - r * ks, k = k0 + kl;
-    float u;
-    if (g.pro == PRO_RMS_X) {
-      u = __ldcg(md.x + static_cast<size_t>(r) * md.H + k) * misc[r] * g.gain[k];
-    } else if (g.pro == PRO_GDN_OUT) {
-      const int hh = k / md.dv, i = k - hh * md.dv;
-      const float o = __ldcg(md.o + static_cast<size_t>(r) * md.o_stride + k);
-      const float z = __ldcg(md.yin + static_cast<size_t>(r) * md.n_in_max + md.conv_ch + k);
-      u = o * misc[r * nh + (hh - h0)] * g.gain[i] * siluf_(z);
-    } else if (g.pro == PRO_FA_OUT) {
-      const float o = __ldcg(md.o + static_cast<size_t>(r) * md.o_stride + k);
-      const float gt = __ldcg(md.yin + static_cast<size_t>(r) * md.n_in_max + md.hq * md.dh + k);
-      u = o * sigmoidf_(gt);
-    } else {
-      u = __ldcg(md.h + static_cast<size_t>(r) * md.F + k);
-    }
-    const __half hi = __float2half_rn(u);
-    const __half lo = __float2half_rn(u - __half2float(hi));
-    const int pos = act_perm(kl);
-    act[(2 * r) * (cstride / 2) + pos] = hi;
-    act[(2 * r + 1) * (cstride / 2) + pos] = lo;
-    float s = warp_sum(__half2float(hi) + __half2float(lo));
-    if (lane == 0) sx[((kl >> 8) * 8 + ((kl & 255) >> 5)) * R + r] = s;
-  }
-  __syncthreads();
-}
-
-// Number of segments (non-empty warp ranges) that touch tile t, over all
-// slices: a unit starts a segment when it is the tile's first unit in its
-// slice or when it belongs to a different warp than the unit before it.
-__device__ int nseg_of_tile(const GemmDesc& g, const Sched& sc, int grid, int64_t t) {
-  int n = 0;
-  for (int sl = 0; sl < sc.S; ++sl) {
-    const int nsb_s = slice_nsb(sc, g.nsb, sl);
-    const int64_t Us = static_cast<int64_t>(g.n_tiles) * nsb_s;
-    const int64_t Ws = static_cast<int64_t>(slice_cta0(sc, grid, sl + 1) - slice_cta0(sc, grid, sl)) * kWarps;
-    int64_t prev = -1;
-    for (int64_t u = t * nsb_s; u < (t + 1) * nsb_s; ++u) {
-      const int64_t w = warp_of_unit(Us, Ws, u);
-      if (w != prev) ++n;
-      prev = w;
-    }
-  }
-  return n;
+  math_sync();
 }
 
 // ------------------------------------------------------------- top-2 state
@@ -430,10 +521,10 @@ __device__ __forceinline__ void top1_merge(float& a1, int& ai, float b1, int bi)
 // --------------------------------------------------------- GEMM epilogue
 template <int NT, bool TOP>
 __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g,
-                                              int64_t tile, const float (&v)[4 * NT], int lane,
+                                              uint32_t tile, const float (&v)[4 * NT], int lane,
                                               Top2<4 * NT>& top) {
   const int R = sd.R;
-  const int64_t n = tile * kTileRows + lane;
+  const int n = static_cast<int>(tile) * kTileRows + lane;
   switch (g.epi) {
     case EPI_STORE_YIN:
       if (n < g.n_out) {
@@ -442,19 +533,22 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
           if (r < R) md.yin[static_cast<size_t>(r) * md.n_in_max + n] = v[r];
       }
       break;
-    case EPI_RESID_X:
-      if (n < md.H) {
+    case EPI_RESID_X: {
+      // H is a multiple of 256, so every lane of the tile holds a real row
 #pragma unroll
-        for (int r = 0; r < 4 * NT; ++r)
-          if (r < R) {
-            float* p = md.x + static_cast<size_t>(r) * md.H + n;
-            *p = __ldcg(p) + v[r];
-          }
-      }
+      for (int r = 0; r < 4 * NT; ++r)
+        if (r < R) {
+          float* p = md.x + static_cast<size_t>(r) * md.H + n;
+          const float xn = __ldcg(p) + v[r];
+          *p = xn;
+          const float sq = warp_sum(xn * xn);  // the next RMSNorm's partial for this 32-wide chunk
+          if (lane == 0) md.xsq[static_cast<size_t>(tile) * kMaxRows + r] = sq;
+        }
       break;
+    }
     case EPI_SWIGLU_H: {
       const int pos = lane & 15;
-      const int64_t f = (tile * 2 + (lane >> 4)) * 8 + (pos & 7);
+      const int f = (static_cast<int>(tile) * 2 + (lane >> 4)) * 8 + (pos & 7);
 #pragma unroll
       for (int r = 0; r < 4 * NT; ++r) {
         const float up = __shfl_down_sync(0xffffffffu, v[r], 8);
@@ -469,7 +563,7 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
           if (r < R) {
             const float x = v[r];
             if (!isfinite(x)) atomicOr(&md.err[1], 1);
-            top1_merge(top.b1[r], top.i1[r], x, static_cast<int>(n));
+            top1_merge(top.b1[r], top.i1[r], x, n);
             if (md.dbg_logits) md.dbg_logits[static_cast<size_t>(r) * md.V + n] = x;
           }
       }
@@ -478,32 +572,75 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
 }
 
 // ------------------------------------------------------------- GEMM phase
-template <int NT>
-__device__ void dequant_word(uint32_t w, const uint4& t, uint32_t (&a)[4]) {
+// One word of 8 codes -> the four A registers of a 16x16 block, exactly: a
+// code masked into the low mantissa bits of an fp16 is the subnormal value
+// q * 2^-24 (rows g, nibbles at bits 0-3 / 16-19) or q * 2^-20 (rows g+8,
+// nibbles at bits 4-7 / 20-23); the tensor core multiplies subnormals
+// exactly, and the per-row factor 2^24 or 2^20 goes into the fp32 scale.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&a)[4]) {
   const uint32_t w8 = w >> 8;
-  a[0] = hfma2_u32(lop3_and_or(w, 0x000F000Fu, 0x64006400u), t.x, t.y);
-  a[1] = hfma2_u32(lop3_and_or(w, 0x00F000F0u, 0x64006400u), t.z, t.w);
-  a[2] = hfma2_u32(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), t.x, t.y);
-  a[3] = hfma2_u32(lop3_and_or(w8, 0x00F000F0u, 0x64006400u), t.z, t.w);
+  a[0] = w & 0x000F000Fu;
+  a[1] = w & 0x00F000F0u;
+  a[2] = w8 & 0x000F000Fu;
+  a[3] = w8 & 0x00F000F0u;
 }
 
+
+// One step of the own-row header decode: sub-block j of the lane's row in
+// the next unit -> its fp32 scale d * sc_j * 2^24 (or 2^20), exact, into the
+// scale table, and the min term dmin * m_j * sum_j(x) added into mtmp.
+template <int NT>
+__device__ __forceinline__ void decode_step(int j, const uint4& hdr, float dscale, float dmin, float* tab, int og,
+                                            int orb, int ohi, const float* sxb, int R, float (&mtmp)[4 * NT]) {
+  const uint32_t f0 = hdr.y, f1 = hdr.z, f2 = hdr.w;
+  uint32_t sc, m;
+  switch (j) {  // 6-bit fields: sc_j at bit 6j, m_j at bit 48 + 6j of the 96-bit field
+    case 0: sc = f0 & 63u; m = (f1 >> 16) & 63u; break;
+    case 1: sc = (f0 >> 6) & 63u; m = (f1 >> 22) & 63u; break;
+    case 2: sc = (f0 >> 12) & 63u; m = __funnelshift_r(f1, f2, 28) & 63u; break;
+    case 3: sc = (f0 >> 18) & 63u; m = (f2 >> 2) & 63u; break;
+    case 4: sc = (f0 >> 24) & 63u; m = (f2 >> 8) & 63u; break;
+    case 5: sc = __funnelshift_r(f0, f1, 30) & 63u; m = (f2 >> 14) & 63u; break;
+    case 6: sc = (f1 >> 4) & 63u; m = (f2 >> 20) & 63u; break;
+    default: sc = (f1 >> 10) & 63u; m = (f2 >> 26) & 63u; break;
+  }
+  tab[j * 32 + og * 4 + orb * 2 + ohi] = dscale * static_cast<float>(sc);  // exact: 11-bit x 6-bit
+  const float dm = dmin * static_cast<float>(m);                          // exact: 11-bit x 6-bit
+#pragma unroll
+  for (int r = 0; r < 4 * NT; ++r)
+    if (r < R) mtmp[r] = fmaf(dm, sxb[j * R + r], mtmp[r]);
+}
+
+// Out of line: each phase function is entered once per phase, and its own
+// register allocation keeps the hot loops free of spills.
+//
+// Per math warp, software-pipelined over its units: while the mma loop of
+// unit k runs, the own-row header decode of unit k+1 fills the other scale
+// table, so neither the decode latency nor the tail of the mma chains stalls
+// the warp.
 template <int NT, bool TOP>
-__device__ __forceinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd, int gp, const Smem& sm,
-                                           WarpCtx& wc) {
+__device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd, int gp, const Smem& sm,
+                                        WarpCtx& wc) {
   const GemmDesc& g = gemm_desc(md, gp);
   const int R = sd.R;
   const int grid = gridDim.x;
   const Assign a = assign_for(g, R, grid, blockIdx.x, wc.warp);
-  produce(wc, md, sd, sm);
   gemm_prologue(md, sd, g, a.sb0, a.nsb_s, sm);
 
   const int lane = wc.lane, gq = lane >> 2, cq = lane & 3;
   const int cstride = act_col_stride(a.nsb_s);
   const uint8_t* act = sm.act();
   const float* sx = reinterpret_cast<const float*>(act + 2 * R * cstride);
-  uint32_t* stab = sm.stab(wc.warp);
-  float* dtab = sm.dtab(wc.warp);
+  // own row of this lane inside a tile: half rb, position og + 8*ohi; its
+  // codes enter the mma as q * 2^-24 (ohi = 0) or q * 2^-20 (ohi = 1)
   const int orb = lane >> 4, opos = lane & 15, og = opos & 7, ohi = opos >> 3;
+  const float row_unscale = ohi ? 1048576.0f : 16777216.0f;  // 2^20 or 2^24
+  const int nsb_s = a.nsb_s;
+  // B column of this lane per column tile; columns past 2R read column 2R-1
+  // (their products land in output columns nobody reads)
+  const uint8_t* bcol[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) bcol[nt] = act + min(nt * 8 + gq, 2 * R - 1) * cstride + cq * 16;
 
   Top2<4 * NT> top;
   if (TOP) {
@@ -512,11 +649,16 @@ __device__ __forceinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& 
   }
 
   float acc[2][NT][4];
-  float mn[4 * NT];
-  int64_t seg_tile = -1, seg_u0 = 0;
+  float mn[4 * NT], mtmp[4 * NT];
+  uint32_t seg_u0 = a.u0;
+#pragma unroll
+  for (int rb = 0; rb < 2; ++rb)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[rb][nt][e] = 0.f;
 
-  auto flush = [&](int64_t tile, int64_t u_end) {
-    float* stage = reinterpret_cast<float*>(stab);  // [32 rows][16 r]
+  auto flush = [&](uint32_t tile, uint32_t u_end, float* stage) {
     __syncwarp();
 #pragma unroll
     for (int rb = 0; rb < 2; ++rb)
@@ -533,10 +675,10 @@ __device__ __forceinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& 
 #pragma unroll
     for (int r = 0; r < 4 * NT; ++r) v[r] = r < R ? stage[lane * 16 + r] - mn[r] : 0.f;
     __syncwarp();
-    const int64_t tu0 = tile * a.nsb_s, tu1 = tu0 + a.nsb_s;
+    const uint32_t tu0 = tile * nsb_s, tu1 = tu0 + nsb_s;
     const bool complete = a.sc.S == 1 && seg_u0 == tu0 && u_end == tu1;
     if (!complete) {
-      const int seg_idx = static_cast<int>(tile - a.u0 / a.nsb_s);
+      const int seg_idx = static_cast<int>(tile - a.u0 / nsb_s);
       float* slot = md.partial + (static_cast<size_t>(wc.gid) * md.max_seg + seg_idx) * kMaxRows * 32;
 #pragma unroll
       for (int r = 0; r < 4 * NT; ++r)
@@ -545,7 +687,14 @@ __device__ __forceinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& 
       __syncwarp();
       uint32_t last = 0;
       if (lane == 0) {
-        const uint32_t n = static_cast<uint32_t>(nseg_of_tile(g, a.sc, grid, tile));
+        uint32_t n = 0;
+        for (int sl = 0; sl < a.sc.S; ++sl) {
+          const uint32_t ns = slice_nsb(a.sc, g.nsb, sl);
+          const uint32_t Us = static_cast<uint32_t>(g.n_tiles) * ns;
+          const uint32_t Ws =
+              static_cast<uint32_t>(slice_cta0(a.sc, grid, sl + 1) - slice_cta0(a.sc, grid, sl)) * kWarps;
+          n += segments_in(Us, Ws, tile * ns, tile * ns + ns);
+        }
         const uint32_t old = atomicAdd(&md.tickets[tile], 1u);
         last = (old + 1u == n) ? 1u : 0u;
         if (last) md.tickets[tile] = 0u;
@@ -556,17 +705,20 @@ __device__ __forceinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& 
 #pragma unroll
       for (int r = 0; r < 4 * NT; ++r) v[r] = 0.f;
       for (int sl = 0; sl < a.sc.S; ++sl) {
-        const int nsb_s = slice_nsb(a.sc, g.nsb, sl);
+        const uint32_t ns = slice_nsb(a.sc, g.nsb, sl);
         const int c0 = slice_cta0(a.sc, grid, sl);
-        const int64_t Us = static_cast<int64_t>(g.n_tiles) * nsb_s;
-        const int64_t Ws = static_cast<int64_t>(slice_cta0(a.sc, grid, sl + 1) - c0) * kWarps;
-        int64_t prev = -1;
-        for (int64_t uu = tile * nsb_s; uu < (tile + 1) * nsb_s; ++uu) {
-          const int64_t ws = warp_of_unit(Us, Ws, uu);
-          if (ws == prev) continue;
-          prev = ws;
+        const uint32_t Us = static_cast<uint32_t>(g.n_tiles) * ns;
+        const uint32_t Ws = static_cast<uint32_t>(slice_cta0(a.sc, grid, sl + 1) - c0) * kWarps;
+        const uint32_t ua = tile * ns, ub = ua + ns;
+        // warps holding units [ua, ub), in order: one per unit when ranges
+        // hold at most one unit, else the consecutive run wf..wl
+        const bool sparse = Us < Ws;
+        const uint32_t first = sparse ? ua : warp_of_unit(Us, Ws, ua);
+        const uint32_t last_w = sparse ? ub - 1 : warp_of_unit(Us, Ws, ub - 1);
+        for (uint32_t it = first; it <= last_w; ++it) {
+          const uint32_t ws = sparse ? warp_of_unit(Us, Ws, it) : it;
           const int gid2 = (c0 + static_cast<int>(ws / kWarps)) * kWarps + static_cast<int>(ws % kWarps);
-          const int seg2 = static_cast<int>(tile - warp_u0(Us, Ws, ws) / nsb_s);
+          const int seg2 = static_cast<int>(tile - warp_u0(Us, Ws, ws) / ns);
           const float* s2 = md.partial + (static_cast<size_t>(gid2) * md.max_seg + seg2) * kMaxRows * 32;
 #pragma unroll
           for (int r = 0; r < 4 * NT; ++r)
@@ -578,108 +730,108 @@ __device__ __forceinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& 
   };
 
   bool ok = true;
-  for (int64_t u = a.u0; u < a.u1; ++u) {
-    const int64_t tile = u / a.nsb_s;
-    const int sbl = static_cast<int>(u - tile * a.nsb_s);
-    if (tile != seg_tile) {
-      if (seg_tile >= 0) flush(seg_tile, u);
-      seg_tile = tile;
-      seg_u0 = u;
+  if (a.u1 > a.u0) {
+    uint32_t tile = a.u0 / nsb_s;
+    int sbl = static_cast<int>(a.u0 - tile * nsb_s);
+    // pipeline fill: decode the first unit
 #pragma unroll
-      for (int rb = 0; rb < 2; ++rb)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[rb][nt][e] = 0.f;
-#pragma unroll
-      for (int r = 0; r < 4 * NT; ++r) mn[r] = 0.f;
-    }
-    if (!wait_unit(wc, sm, md, sd.barrier_timeout_ns)) { ok = false; break; }
-    const uint8_t* unit = sm.ring(wc.warp, wc.c_pos % kRing);
-    // --- own row: scale table, d table and the min term
-    {
+    for (int r = 0; r < 4 * NT; ++r) mtmp[r] = 0.f;
+    if (!wait_unit(wc, sm, md, sd.barrier_timeout_ns)) {
+      ok = false;
+    } else {
+      const uint8_t* unit = sm.ring(wc.warp, wc.c_pos % kRing);
       const uint4 hdr = *reinterpret_cast<const uint4*>(unit + 16 * lane);
       const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
       const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-      const uint64_t lo64 = hdr.y | (static_cast<uint64_t>(hdr.z) << 32);
-      const uint64_t mid64 = hdr.z | (static_cast<uint64_t>(hdr.w) << 32);
+      float* tab = reinterpret_cast<float*>(sm.stab(wc.warp, 0));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float scf = static_cast<float>(static_cast<uint32_t>(lo64 >> (6 * j)) & 63u);
-        const float mf = static_cast<float>(static_cast<uint32_t>(mid64 >> (16 + 6 * j)) & 63u);
-        __half2 s2, b2;
-        if (ohi == 0) {
-          s2 = __float2half2_rn(scf);
-          b2 = __float2half2_rn(-1024.f * scf);
-        } else {
-          s2 = __float2half2_rn(scf * 0.0625f);
-          b2 = __float2half2_rn(-64.f * scf);
+      for (int j = 0; j < 8; ++j)
+        decode_step<NT>(j, hdr, d * row_unscale, dmin, tab, og, orb, ohi, sx + sbl * 8 * R, R, mtmp);
+    }
+#pragma unroll
+    for (int r = 0; r < 4 * NT; ++r) mn[r] = mtmp[r];
+    __syncwarp();
+    for (uint32_t u = a.u0; ok && u < a.u1; ++u) {
+      const int cur = static_cast<int>((u - a.u0) & 1u);
+      const bool has_next = u + 1 < a.u1;
+      const int sbl_next = sbl + 1 == nsb_s ? 0 : sbl + 1;
+      const uint8_t* unit = sm.ring(wc.warp, wc.c_pos % kRing);
+      const float* tab = reinterpret_cast<const float*>(sm.stab(wc.warp, cur));
+      float* tabn = reinterpret_cast<float*>(sm.stab(wc.warp, cur ^ 1));
+      uint4 hdrn = make_uint4(0u, 0u, 0u, 0u);
+      float dscalen = 0.f, dminn = 0.f;
+      if (has_next) {
+        WarpCtx nx = wc;
+        ++nx.c_pos;
+        if (!wait_unit(nx, sm, md, sd.barrier_timeout_ns)) { ok = false; break; }
+        hdrn = *reinterpret_cast<const uint4*>(sm.ring(wc.warp, nx.c_pos % kRing) + 16 * lane);
+        dscalen = __half2float(__ushort_as_half(static_cast<unsigned short>(hdrn.x & 0xffffu))) * row_unscale;
+        dminn = __half2float(__ushort_as_half(static_cast<unsigned short>(hdrn.x >> 16)));
+      }
+#pragma unroll
+      for (int r = 0; r < 4 * NT; ++r) mtmp[r] = 0.f;
+      const uint8_t* codes = unit + kUnitHdr + lane * 16;
+      const int boff = sbl * 512;
+      const float* sxn = sx + sbl_next * 8 * R;
+#pragma unroll
+      for (int kp = 0; kp < 8; ++kp) {
+        const uint4 w4 = *reinterpret_cast<const uint4*>(codes + kp * 512);
+        // fp32 scales of rows (g, g+8) of both 16-row halves for sub-block kp
+        const float4 s4 = *reinterpret_cast<const float4*>(tab + kp * 32 + gq * 4);
+        uint4 bf[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          bf[nt] = *reinterpret_cast<const uint4*>(bcol[nt] + boff + kp * 64);
+        float t0[NT][4], t1[NT][4];  // sub-block sums of halves 0 and 1 (two k-steps each)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) t0[nt][e] = t1[nt][e] = 0.f;
+        uint32_t av[4];
+        dequant_word(w4.x, av);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(t0[nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
+        dequant_word(w4.y, av);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(t1[nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
+        dequant_word(w4.z, av);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(t0[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
+        dequant_word(w4.w, av);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(t1[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
+        if (has_next) decode_step<NT>(kp, hdrn, dscalen, dminn, tabn, og, orb, ohi, sxn, R, mtmp);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[0][nt][0] = fmaf(s4.x, t0[nt][0], acc[0][nt][0]);
+          acc[0][nt][1] = fmaf(s4.x, t0[nt][1], acc[0][nt][1]);
+          acc[0][nt][2] = fmaf(s4.y, t0[nt][2], acc[0][nt][2]);
+          acc[0][nt][3] = fmaf(s4.y, t0[nt][3], acc[0][nt][3]);
+          acc[1][nt][0] = fmaf(s4.z, t1[nt][0], acc[1][nt][0]);
+          acc[1][nt][1] = fmaf(s4.z, t1[nt][1], acc[1][nt][1]);
+          acc[1][nt][2] = fmaf(s4.w, t1[nt][2], acc[1][nt][2]);
+          acc[1][nt][3] = fmaf(s4.w, t1[nt][3], acc[1][nt][3]);
         }
-        uint32_t* e = stab + ((j * 8 + og) * 2 + orb) * 4 + 2 * ohi;
-        e[0] = h2u(s2);
-        e[1] = h2u(b2);
-        const float dm = dmin * mf;  // exact: 11-bit x 6-bit
-        const float* sxj = sx + (sbl * 8 + j) * R;
-#pragma unroll
-        for (int r = 0; r < 4 * NT; ++r)
-          if (r < R) mn[r] = fmaf(dm, sxj[r], mn[r]);
       }
-      dtab[og * 4 + orb * 2 + ohi] = d;
-    }
-    __syncwarp();
-    float tmp[2][NT][4];
+      release_unit(wc, sm);  // includes __syncwarp: both tables are settled
+      if (++sbl == nsb_s || u + 1 == a.u1) {
+        flush(tile, u + 1, reinterpret_cast<float*>(sm.stab(wc.warp, cur)));
+        seg_u0 = u + 1;
 #pragma unroll
-    for (int rb = 0; rb < 2; ++rb)
+        for (int rb = 0; rb < 2; ++rb)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) tmp[rb][nt][e] = 0.f;
-    const uint8_t* codes = unit + kUnitHdr;
-#pragma unroll (NT <= 2 ? 2 : 1)
-    for (int kp = 0; kp < 8; ++kp) {
-      const uint4 w4 = *reinterpret_cast<const uint4*>(codes + kp * 512 + lane * 16);
-      const uint4 t0 = *reinterpret_cast<const uint4*>(stab + ((kp * 8 + gq) * 2 + 0) * 4);
-      const uint4 t1 = *reinterpret_cast<const uint4*>(stab + ((kp * 8 + gq) * 2 + 1) * 4);
-      uint4 bf[NT];
+            for (int e = 0; e < 4; ++e) acc[rb][nt][e] = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int col = nt * 8 + gq;
-        if (col < 2 * R)
-          bf[nt] = *reinterpret_cast<const uint4*>(act + col * cstride + (sbl * 256 + kp * 32) * 2 + cq * 16);
-        else
-          bf[nt] = make_uint4(0u, 0u, 0u, 0u);
+        for (int r = 0; r < 4 * NT; ++r) mn[r] = 0.f;
+        if (sbl == nsb_s) { sbl = 0; ++tile; }
       }
-      uint32_t av[4];
-      dequant_word<NT>(w4.x, t0, av);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816(tmp[0][nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
-      dequant_word<NT>(w4.y, t1, av);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816(tmp[1][nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
-      dequant_word<NT>(w4.z, t0, av);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816(tmp[0][nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
-      dequant_word<NT>(w4.w, t1, av);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816(tmp[1][nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
+      for (int r = 0; r < 4 * NT; ++r) mn[r] += mtmp[r];
+      __syncwarp();
     }
-    const float4 d4 = *reinterpret_cast<const float4*>(dtab + gq * 4);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      acc[0][nt][0] = fmaf(d4.x, tmp[0][nt][0], acc[0][nt][0]);
-      acc[0][nt][1] = fmaf(d4.x, tmp[0][nt][1], acc[0][nt][1]);
-      acc[0][nt][2] = fmaf(d4.y, tmp[0][nt][2], acc[0][nt][2]);
-      acc[0][nt][3] = fmaf(d4.y, tmp[0][nt][3], acc[0][nt][3]);
-      acc[1][nt][0] = fmaf(d4.z, tmp[1][nt][0], acc[1][nt][0]);
-      acc[1][nt][1] = fmaf(d4.z, tmp[1][nt][1], acc[1][nt][1]);
-      acc[1][nt][2] = fmaf(d4.w, tmp[1][nt][2], acc[1][nt][2]);
-      acc[1][nt][3] = fmaf(d4.w, tmp[1][nt][3], acc[1][nt][3]);
-    }
-    __syncwarp();
-    ++wc.c_pos;
-    produce(wc, md, sd, sm);
   }
-  if (ok && seg_tile >= 0) flush(seg_tile, a.u1);
 
   if (TOP) {
     // warp-level merge, then one record per warp
@@ -703,7 +855,7 @@ __device__ __forceinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& 
 }
 
 __device__ __forceinline__ bool gemm_dispatch(const ModelDesc& md, const StepDesc& sd, int gp, const Smem& sm,
-                                           WarpCtx& wc) {
+                                              WarpCtx& wc) {
   const bool top = (gp >> 2) >= md.n_layers;
   switch (sd.nt) {
     case 1: return top ? gemm_phase<1, true>(md, sd, gp, sm, wc) : gemm_phase<1, false>(md, sd, gp, sm, wc);
@@ -719,7 +871,7 @@ __device__ __forceinline__ bool gemm_dispatch(const ModelDesc& md, const StepDes
 //   S_i <- alpha S_i + beta (v_i - alpha S_i.k) k,   o_i = S_i.q,
 // writing the state after each row into that row's snapshot slot (the commit
 // later selects one). Rows of S are independent, so tasks never communicate.
-__device__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const WarpCtx& wc, const Smem& sm) {
+__device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const WarpCtx& wc, const Smem& sm) {
   const LayerDesc& L = md.layer[layer];
   const int gi = L.gdn_i;
   const int hk = md.hk, hv = md.hv, dk = md.dk, dv = md.dv, C = md.conv_ch;
@@ -750,9 +902,11 @@ __device__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, int layer, co
       return siluf_(c);
     };
     // normalised q, k of this head for every row: [t][dk] each, per warp
-    float* qs = reinterpret_cast<float*>(sm.phase()) + wc.warp * (2 * kMaxT * 128);
+    float* qs = reinterpret_cast<float*>(sm.phase()) + wc.warp * (2 * kMaxT * 128 + kMaxT * 10);
     float* ks = qs + kMaxT * 128;
-    float vv[kMaxT], al[kMaxT], be[kMaxT];
+    // per-row gates and this task's 8 v values: [t] in shared memory after q, k
+    float* vs = ks + kMaxT * 128;  // [kMaxT][8]
+    float* gs = vs + kMaxT * 8;    // [kMaxT][2] alpha, beta
 #pragma unroll
     for (int t = 0; t < kMaxT; ++t) {
       if (t < T) {
@@ -778,50 +932,75 @@ __device__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, int layer, co
             qs[t * 128 + lane + 32 * e] = q4[e] * iq;
             ks[t * 128 + lane + 32 * e] = k4[e] * ik;
           }
-        vv[t] = lane < 8 ? conv(2 * hk * dk + h * dv + i0 + lane, t) : 0.f;
-        const float* yr = md.yin + static_cast<size_t>(row0 + t) * md.n_in_max;
-        al[t] = sigmoidf_(__ldcg(yr + a_off + h));
-        be[t] = sigmoidf_(__ldcg(yr + b_off + h));
+        if (lane < 8) vs[t * 8 + lane] = conv(2 * hk * dk + h * dv + i0 + lane, t);
+        if (lane == 0) {
+          const float* yr = md.yin + static_cast<size_t>(row0 + t) * md.n_in_max;
+          gs[t * 2 + 0] = sigmoidf_(__ldcg(yr + a_off + h));
+          gs[t * 2 + 1] = sigmoidf_(__ldcg(yr + b_off + h));
+        }
       }
     }
     __syncwarp();
     const float* Sin = md.gdn_state + ((seq_slot_in * md.n_gdn + gi) * hv + h) * static_cast<size_t>(dv) * dk;
-    for (int ii = 0; ii < 8; ++ii) {
-      const int i = i0 + ii;
-      float s[4];
+    // the task's 8 state rows, loaded at once (independent rows of S)
+    float s[8][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[e] = e < ne ? __ldcg(Sin + static_cast<size_t>(i) * dk + lane + 32 * e) : 0.f;
+    for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
-      for (int t = 0; t < kMaxT; ++t) {
-        if (t < T) {
-          float kt[4], qt[4];
+      for (int e = 0; e < 4; ++e)
+        s[ii][e] = e < ne ? __ldcg(Sin + static_cast<size_t>(i0 + ii) * dk + lane + 32 * e) : 0.f;
+    for (int t = 0; t < T; ++t) {
+      float kt[4], qt[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            kt[e] = e < ne ? ks[t * 128 + lane + 32 * e] : 0.f;
-            qt[e] = e < ne ? qs[t * 128 + lane + 32 * e] : 0.f;
-          }
-          float sk = 0.f;
+      for (int e = 0; e < 4; ++e) {
+        kt[e] = e < ne ? ks[t * 128 + lane + 32 * e] : 0.f;
+        qt[e] = e < ne ? qs[t * 128 + lane + 32 * e] : 0.f;
+      }
+      const float al = gs[t * 2 + 0], be = gs[t * 2 + 1];
+      const bool snap = sd.seq_snap_all[si] || t == T - 1;
+      float* So = nullptr;
+      if (snap) {
+        const size_t ss = static_cast<size_t>(seq) * md.n_slots + sd.seq_slot_out[si][t];
+        So = md.gdn_state + ((ss * md.n_gdn + gi) * hv + h) * static_cast<size_t>(dv) * dk;
+      }
+      float skv[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sk = fmaf(s[e], kt[e], sk);
-          sk = warp_sum(sk);
-          const float vi = __shfl_sync(0xffffffffu, vv[t], ii);
-          const float delta = be[t] * (vi - al[t] * sk);
+      for (int ii = 0; ii < 8; ++ii) {
+        float a = 0.f;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) s[e] = fmaf(al[t], s[e], delta * kt[e]);
-          float so = 0.f;
+        for (int e = 0; e < 4; ++e) a = fmaf(s[ii][e], kt[e], a);
+        skv[ii] = a;
+      }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) so = fmaf(s[e], qt[e], so);
-          so = warp_sum(so);
-          if (lane == 0) md.o[static_cast<size_t>(row0 + t) * md.o_stride + h * dv + i] = so;
-          if (sd.seq_snap_all[si] || t == T - 1) {
-            const size_t ss = static_cast<size_t>(seq) * md.n_slots + sd.seq_slot_out[si][t];
-            float* So = md.gdn_state + ((ss * md.n_gdn + gi) * hv + h) * static_cast<size_t>(dv) * dk +
-                        static_cast<size_t>(i) * dk;
+      for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (e < ne) __stcg(So + lane + 32 * e, s[e]);
-          }
+        for (int ii = 0; ii < 8; ++ii) skv[ii] += __shfl_xor_sync(0xffffffffu, skv[ii], o);
+      float sov[8];
+#pragma unroll
+      for (int ii = 0; ii < 8; ++ii) {
+        const float delta = be * (vs[t * 8 + ii] - al * skv[ii]);
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s[ii][e] = fmaf(al, s[ii][e], delta * kt[e]);
+          a = fmaf(s[ii][e], qt[e], a);
         }
+        sov[ii] = a;
+        if (snap) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (e < ne) __stcg(So + static_cast<size_t>(i0 + ii) * dk + lane + 32 * e, s[ii][e]);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) sov[ii] += __shfl_xor_sync(0xffffffffu, sov[ii], o);
+      if (lane < 8) {
+        float ov = sov[0];
+#pragma unroll
+        for (int ii = 1; ii < 8; ++ii) ov = lane == ii ? sov[ii] : ov;
+        md.o[static_cast<size_t>(row0 + t) * md.o_stride + h * dv + i0 + lane] = ov;
       }
     }
     // convolution history after each row, for the channels this task owns
@@ -898,7 +1077,7 @@ __device__ void attn_store_kv(const ModelDesc& md, int fa_i, int page, int kh, i
   }
 }
 
-__device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const Smem& sm, float* scratch_row) {
+__device__ __noinline__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const Smem& sm, float* scratch_row) {
   const LayerDesc& L = md.layer[layer];
   const int fa_i = L.fa_i;
   const int dh = md.dh, hkv = md.hkv, grp = md.hq / md.hkv;
@@ -916,6 +1095,7 @@ __device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, c
   as.l = as.m + kMaxQRows;
   as.sc = as.l + kMaxQRows;
   as.flag = reinterpret_cast<int*>(as.sc + kMaxQRows);
+  float* wbuf = reinterpret_cast<float*>(as.flag + 4);  // [kWarps][kMaxSplits] split weights
   const float inv_sqrt_dh = 1.0f / sqrtf(static_cast<float>(dh));
   const int kq_off = 2 * md.hq * dh;           // k after q and gate
   const int vq_off = kq_off + hkv * dh;         // v after k
@@ -962,42 +1142,75 @@ __device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, c
       for (int b = 0; b < 4; ++b)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
-    __syncthreads();
+    math_sync();
 
     const int n_iter = (te - tb) + (last ? 1 : 0);
-    for (int it = 0; it < n_iter; ++it) {
-      const bool newtile = last && it == n_iter - 1;
-      const int tile = tb + it;
-      // ---- load K/V tile (32 tokens) as fp16
-      if (!newtile) {
-        const int vec_per_row = dh / 8;  // 16-byte vectors of 8 halves
-        for (int idx = tid; idx < 2 * 32 * vec_per_row; idx += kThreads) {
+    // K/V tile staging: each thread holds up to 8 raw 16-byte (fp16) or
+    // 8-byte (q8, plus its block scale) vectors of the NEXT cached tile in
+    // registers, so the tile's load latency overlaps the current tile's work.
+    const int vec_per_row = dh / 8;
+    const int nvec = 2 * 32 * vec_per_row;  // K and V rows of 32 tokens
+    uint4 pf[8];
+    uint16_t pfs[8];
+    auto load_tile = [&](int tile) {
+#pragma unroll
+      for (int jv = 0; jv < 8; ++jv) {
+        const int idx = tid + jv * kThreads;
+        pf[jv] = make_uint4(0u, 0u, 0u, 0u);
+        pfs[jv] = 0;
+        if (idx < nvec) {
           const int which = idx / (32 * vec_per_row);
           const int rem = idx % (32 * vec_per_row);
           const int tk = rem / vec_per_row, vi = rem % vec_per_row;
           const int tok = tile * 32 + tk;
-          __half* dst = (which ? as.V : as.K) + tk * dpad + vi * 8;
-          uint4 val = make_uint4(0u, 0u, 0u, 0u);
           if (tok < Lc) {
             const int page = pt[tok / md.page_tokens], slot = tok % md.page_tokens;
             const size_t row = ((static_cast<size_t>(fa_i) * md.n_pages + page) * hkv + kh) * md.page_tokens + slot;
             if (!md.kv_q8) {
-              const __half* src = reinterpret_cast<const __half*>(which ? md.kv_v : md.kv_k) + row * dh + vi * 8;
-              val = __ldcg(reinterpret_cast<const uint4*>(src));
+              pf[jv] = __ldcg(reinterpret_cast<const uint4*>(
+                  reinterpret_cast<const __half*>(which ? md.kv_v : md.kv_k) + row * dh + vi * 8));
             } else {
-              const int8_t* src = reinterpret_cast<const int8_t*>(which ? md.kv_v : md.kv_k) + row * dh + vi * 8;
-              const uint2 c8 = __ldcg(reinterpret_cast<const uint2*>(src));
-              const uint16_t sbits = __ldcg((which ? md.kv_vs : md.kv_ks) + row * (dh / 32) + (vi * 8) / 32);
-              const float d16 = __half2float(__ushort_as_half(sbits));
-              __half hv[8];
-              const int8_t* cb = reinterpret_cast<const int8_t*>(&c8);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) hv[e] = __float2half_rn(d16 * static_cast<float>(cb[e]));
-              val = *reinterpret_cast<uint4*>(hv);
+              const uint2 c8 = __ldcg(reinterpret_cast<const uint2*>(
+                  reinterpret_cast<const int8_t*>(which ? md.kv_v : md.kv_k) + row * dh + vi * 8));
+              pf[jv].x = c8.x;
+              pf[jv].y = c8.y;
+              pfs[jv] = __ldcg((which ? md.kv_vs : md.kv_ks) + row * (dh / 32) + (vi * 8) / 32);
             }
+          }
+        }
+      }
+    };
+    auto store_tile = [&]() {
+#pragma unroll
+      for (int jv = 0; jv < 8; ++jv) {
+        const int idx = tid + jv * kThreads;
+        if (idx < nvec) {
+          const int which = idx / (32 * vec_per_row);
+          const int rem = idx % (32 * vec_per_row);
+          const int tk = rem / vec_per_row, vi = rem % vec_per_row;
+          __half* dst = (which ? as.V : as.K) + tk * dpad + vi * 8;
+          uint4 val = pf[jv];
+          if (md.kv_q8) {
+            // masked tokens stay zero: their codes and scale were never loaded
+            const float d16 = __half2float(__ushort_as_half(pfs[jv]));
+            const int8_t* cb = reinterpret_cast<const int8_t*>(&pf[jv]);
+            __half hv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hv[e] = __float2half_rn(d16 * static_cast<float>(cb[e]));
+            val = *reinterpret_cast<uint4*>(hv);
           }
           *reinterpret_cast<uint4*>(dst) = val;
         }
+      }
+    };
+    if (te > tb) load_tile(tb);
+    for (int it = 0; it < n_iter; ++it) {
+      const bool newtile = last && it == n_iter - 1;
+      const int tile = tb + it;
+      // ---- K/V tile (32 tokens) as fp16
+      if (!newtile) {
+        store_tile();
+        if (tile + 1 < te) load_tile(tile + 1);
       } else {
         // this step's own keys/values: RoPE k, round or quantise, append, keep as the tile
         for (int idx = tid; idx < 32 * dh; idx += kThreads) {
@@ -1027,7 +1240,7 @@ __device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, c
           __syncwarp();
         }
       }
-      __syncthreads();
+      math_sync();
       // ---- S = Q K^T (scaled already)
       for (int unit = warp; unit < mt * 4; unit += kWarps) {
         const int mi = unit / 4, ni = unit % 4;
@@ -1048,7 +1261,7 @@ __device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, c
         as.S[(r0 + 8) * 33 + c0] = s4[2];
         as.S[(r0 + 8) * 33 + c0 + 1] = s4[3];
       }
-      __syncthreads();
+      math_sync();
       // ---- online softmax, one row per warp iteration, lane = token
       for (int qr = warp; qr < mt * 16; qr += kWarps) {
         float p = 0.f, scl = 1.f;
@@ -1077,7 +1290,7 @@ __device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, c
         as.P[qr * 40 + lane] = __float2half_rn(p);
         if (lane == 0) as.sc[qr] = scl;
       }
-      __syncthreads();
+      math_sync();
       // ---- acc = acc * scale + P V  (warp w owns dims [w*nd, (w+1)*nd))
 #pragma unroll
       for (int mi = 0; mi < 3; ++mi) {
@@ -1111,7 +1324,7 @@ __device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, c
           }
         }
       }
-      __syncthreads();
+      math_sync();
     }
 
     // ---- write out: directly if one split, else partial + last-block combine
@@ -1155,7 +1368,7 @@ __device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, c
         __stcg(part + qr * (kMaxDh + 2) + kMaxDh + 1, as.l[qr]);
       }
       __threadfence();
-      __syncthreads();
+      math_sync();
       if (tid == 0) {
         const int key = si * hkv + kh;
         const uint32_t old = atomicAdd(&md.attn_tickets[key], 1u);
@@ -1163,31 +1376,56 @@ __device__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, c
         if (is_last) md.attn_tickets[key] = 0u;
         *as.flag = is_last;
       }
-      __syncthreads();
+      math_sync();
       if (*as.flag) {
         __threadfence();
         const int item0 = sd.seq_item0[si] + kh * nsplit;
-        for (int idx = tid; idx < qrows * dh; idx += kThreads) {
-          const int qr = idx / dh, d = idx % dh;
-          float M = -INFINITY;
-          for (int s = 0; s < nsplit; ++s)
-            M = fmaxf(M, __ldcg(md.attn_part + (static_cast<size_t>(item0 + s) * kMaxQRows + qr) * (kMaxDh + 2) + kMaxDh));
-          float Ls = 0.f, val = 0.f;
-          for (int s = 0; s < nsplit; ++s) {
-            const float* p = md.attn_part + (static_cast<size_t>(item0 + s) * kMaxQRows + qr) * (kMaxDh + 2);
-            const float ms = __ldcg(p + kMaxDh);
+        float* wb = wbuf + warp * kMaxSplits;
+        // one warp per query row: split weights over lanes, head dims over lanes
+        for (int qr = warp; qr < qrows; qr += kWarps) {
+          float mloc = -INFINITY;
+          for (int sp = lane; sp < nsplit; sp += 32)
+            mloc = fmaxf(mloc, __ldcg(md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + qr) * (kMaxDh + 2) + kMaxDh));
+          const float M = warp_max(mloc);
+          float lloc = 0.f;
+          for (int sp = lane; sp < nsplit; sp += 32) {
+            const float* pp = md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + qr) * (kMaxDh + 2);
+            const float ms = __ldcg(pp + kMaxDh);
             const float w = ms == -INFINITY ? 0.f : expf(ms - M);
-            Ls = fmaf(__ldcg(p + kMaxDh + 1), w, Ls);
-            val = fmaf(__ldcg(p + d), w, val);
+            wb[sp] = w;
+            lloc = fmaf(__ldcg(pp + kMaxDh + 1), w, lloc);
+          }
+          const float inv = 1.0f / warp_sum(lloc);
+          __syncwarp();
+          float val[kMaxDh / 32];
+#pragma unroll
+          for (int e = 0; e < kMaxDh / 32; ++e) val[e] = 0.f;
+#pragma unroll 4
+          for (int sp = 0; sp < nsplit; ++sp) {
+            const float w = wb[sp];
+            const float* pp = md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + qr) * (kMaxDh + 2);
+#pragma unroll
+            for (int e = 0; e < kMaxDh / 32; ++e)
+              if (lane + 32 * e < dh) val[e] = fmaf(__ldcg(pp + lane + 32 * e), w, val[e]);
           }
           const int t = qr / grp, hh = kh * grp + qr % grp;
-          md.o[static_cast<size_t>(row0 + t) * md.o_stride + hh * dh + d] = val / Ls;
+          float* o = md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh;
+#pragma unroll
+          for (int e = 0; e < kMaxDh / 32; ++e)
+            if (lane + 32 * e < dh) o[lane + 32 * e] = val[e] * inv;
+          __syncwarp();
         }
       }
     }
-    __syncthreads();
+    math_sync();
   }
 }
+
+static_assert(kMaxQRows * (kMaxDh + 8) * 2 + 2 * 32 * (kMaxDh + 8) * 2 + kMaxQRows * 33 * 4 + kMaxQRows * 40 * 2 +
+                      3 * kMaxQRows * 4 + 16 + kWarps * kMaxSplits * 4 <=
+                  kPhaseBytes,
+              "attention shared memory");
+static_assert(kWarps * (2 * kMaxT * 128 + kMaxT * 10) * 4 <= kPhaseBytes, "Gated DeltaNet shared memory");
 
 // ------------------------------------------------------------------ verify
 // Block 0: argmax of every row over all warps' top-2 records (lowest index on
@@ -1214,7 +1452,7 @@ __device__ void verify_phase(const ModelDesc& md, const StepDesc& sd, const Smem
     }
     if (lane == 0) am[r] = i1;
   }
-  __syncthreads();
+  math_sync();
   if (tid == 0) {
     int at = 0;
     for (int si = 0; si < sd.n_seq; ++si) {
@@ -1233,35 +1471,37 @@ __device__ void verify_phase(const ModelDesc& md, const StepDesc& sd, const Smem
 }
 
 // ------------------------------------------------------------- the kernel
-__global__ void __launch_bounds__(kThreads, 1)
+// 9 warps: at most 168 registers each (three warps share a sub-partition).
+__global__ void __launch_bounds__(kLaunchThreads, 1)
     mk_persistent(const ModelDesc* __restrict__ mdp, const StepDesc* __restrict__ sdp, float* attn_scratch) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ int sflag;
   const Smem sm{smem_raw};
   const ModelDesc& md = *mdp;
   const StepDesc& sd = *sdp;
-  WarpCtx wc;
-  wc.warp = threadIdx.x >> 5;
-  wc.lane = threadIdx.x & 31;
-  wc.gid = blockIdx.x * kWarps + wc.warp;
-  wc.c_pos = wc.p_pos = 0;
-  wc.p_gp = -1;
-  wc.p_done = false;
-  wc.p_u = wc.p_u1 = 0;
-  wc.p_nsb_s = wc.p_sb0 = wc.p_nsb = 1;
-  wc.p_w = nullptr;
-  wc.pol = evict_first_policy();
-  if (wc.lane == 0)
-    for (int s = 0; s < kRing; ++s) mbar_init(sm.bar(wc.warp, s), 1);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x < kWarps * kRing) {
+    mbar_init(sm.bar(threadIdx.x / kRing, threadIdx.x % kRing), 1);
+    mbar_init(sm.empty(threadIdx.x / kRing, threadIdx.x % kRing), 1);
+  }
   mbar_fence_init();
   __syncthreads();
+  if (warp == kWarps) {  // the producer warp
+    producer_warp(md, sd, sm);
+    return;
+  }
+  WarpCtx wc;
+  wc.warp = warp;
+  wc.lane = threadIdx.x & 31;
+  wc.gid = blockIdx.x * kWarps + wc.warp;
+  wc.c_pos = 0;
 
   int nbar = 0;
   float* my_scratch = attn_scratch + static_cast<size_t>(blockIdx.x) * kWarps * 2 * kMaxDh;
-  produce(wc, md, sd, sm);
   // Phases: 0 embed; then per layer l: 1+5l input GEMM, 2+5l mixer,
   // 3+5l o_proj, 4+5l gate/up, 5+5l down; then lm_head; then verify.
   const int n_phases = 1 + 5 * md.n_layers + 2;
+  if (md.dbg_time && blockIdx.x == 0 && threadIdx.x == 0) md.dbg_time[0] = globaltimer();
   for (int ph = 0; ph < n_phases; ++ph) {
     bool ok = true;
     int gp = -1;
@@ -1275,7 +1515,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       const int l = (ph - 1) / 5, part = (ph - 1) % 5;
       if (part == 1) {
-        produce(wc, md, sd, sm);
         if (md.layer[l].kind == MK_LAYER_GDN) gdn_phase(md, sd, l, wc, sm);
         else attn_phase(md, sd, l, sm, my_scratch);
       } else {
@@ -1284,16 +1523,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (gp >= 0) ok = gemm_dispatch(md, sd, gp, sm, wc);
     // a failed wait inside a phase still meets the barrier, which reports it
-    if (!grid_sync(md, sd, nbar, &sflag) || !ok) break;
+    const bool synced = grid_sync(md, sd, nbar, &sflag);
+    if (md.dbg_time && blockIdx.x == 0 && threadIdx.x == 0) md.dbg_time[ph + 1] = globaltimer();
+    if (!synced || !ok) break;
   }
-  drain(wc, sm, md);
 }
 
 cudaError_t launch_persistent(const ModelDesc* md, const StepDesc* sd, float* attn_scratch, int grid,
                               cudaStream_t stream) {
   void* args[] = {const_cast<ModelDesc**>(&md), const_cast<StepDesc**>(&sd), &attn_scratch};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(mk_persistent), dim3(grid), dim3(kThreads), args,
-                                     kSmemBytes, stream);
+  return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(mk_persistent), dim3(grid), dim3(kLaunchThreads),
+                                     args, kSmemBytes, stream);
 }
 
 cudaError_t configure_persistent(int* blocks_per_sm) {
@@ -1301,7 +1541,7 @@ cudaError_t configure_persistent(int* blocks_per_sm) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, reinterpret_cast<const void*>(mk_persistent),
-                                                       kThreads, kSmemBytes);
+                                                       kLaunchThreads, kSmemBytes);
 }
 
 }  // namespace mk

@@ -12,7 +12,7 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmk.so")
+LIB_PATH = os.environ.get("MK_LIBRARY", os.path.join(_HERE, "libmk.so"))
 
 MK_MAX_LAYERS = 64
 MK_MAX_SEQS = 8
@@ -92,6 +92,7 @@ def _load():
         "mk_debug_scratch": (i32, [vp, i32, vp, vp, vp, vp, P(i32), P(i32)]),
         "mk_step_io_bytes": (i32, [vp, P(u64), P(u64)]),
         "mk_step_static": (i32, [vp, i32, vp, vp, vp, vp, vp, vp]),
+        "mk_debug_timeline": (i32, [vp, vp]),
         "mk_status_str": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -107,7 +108,8 @@ EXPORTS = ["mk_packed_bytes", "mk_kv_bytes", "mk_kv_scale_bytes", "mk_gdn_state_
            "mk_conv_state_bytes", "mk_create", "mk_free", "mk_seq_set", "mk_seq_reset", "mk_seq_get",
            "mk_step", "mk_step_prepare", "mk_step_launch", "mk_step_finish", "mk_commit",
            "mk_debug_outputs", "mk_last_launch_ms", "mk_debug_skip_arrival", "mk_grid_blocks",
-           "mk_status_str", "mk_debug_scratch", "mk_step_io_bytes", "mk_step_static"]
+           "mk_status_str", "mk_debug_scratch", "mk_step_io_bytes", "mk_step_static",
+           "mk_debug_timeline"]
 
 
 def _np_ptr(a):
@@ -312,6 +314,10 @@ class Engine:
     def debug_outputs(self, logits=None, hidden=None):
         _check(lib.mk_debug_outputs(self.ctx, None if logits is None else logits.data_ptr(),
                                     None if hidden is None else hidden.data_ptr()), "mk_debug_outputs")
+
+    def timeline(self, stamps=None):
+        """Enable (int64 CUDA tensor of >= 5*n_layers+4 entries) or disable the phase timeline."""
+        _check(lib.mk_debug_timeline(self.ctx, None if stamps is None else stamps.data_ptr()), "mk_debug_timeline")
 
     def skip_arrival(self, block: int, barrier: int, timeout_ns: int = 0):
         _check(lib.mk_debug_skip_arrival(self.ctx, block, barrier, timeout_ns), "mk_debug_skip_arrival")
