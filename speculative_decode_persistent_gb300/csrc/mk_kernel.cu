@@ -590,8 +590,8 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&a)[4]) {
 // the next unit -> its fp32 scale d * sc_j * 2^24 (or 2^20), exact, into the
 // scale table, and the min term dmin * m_j * sum_j(x) added into mtmp.
 template <int NT>
-__device__ __forceinline__ void decode_step(int j, const uint4& hdr, float dscale, float dmin, float* tab, int og,
-                                            int orb, int ohi, const float* sxb, int R, float (&mtmp)[4 * NT]) {
+__device__ __forceinline__ float decode_step(int j, const uint4& hdr, float dscale, float dmin, const float* sxb,
+                                             int R, float (&mtmp)[4 * NT]) {
   const uint32_t f0 = hdr.y, f1 = hdr.z, f2 = hdr.w;
   uint32_t sc, m;
   switch (j) {  // 6-bit fields: sc_j at bit 6j, m_j at bit 48 + 6j of the 96-bit field
@@ -604,11 +604,18 @@ __device__ __forceinline__ void decode_step(int j, const uint4& hdr, float dscal
     case 6: sc = (f1 >> 4) & 63u; m = (f2 >> 20) & 63u; break;
     default: sc = (f1 >> 10) & 63u; m = (f2 >> 26) & 63u; break;
   }
-  tab[j * 32 + og * 4 + orb * 2 + ohi] = dscale * static_cast<float>(sc);  // exact: 11-bit x 6-bit
-  const float dm = dmin * static_cast<float>(m);                          // exact: 11-bit x 6-bit
+  const float dm = dmin * static_cast<float>(m);  // exact: 11-bit x 6-bit
 #pragma unroll
   for (int r = 0; r < 4 * NT; ++r)
     if (r < R) mtmp[r] = fmaf(dm, sxb[j * R + r], mtmp[r]);
+  return dscale * static_cast<float>(sc);  // exact: 11-bit x 6-bit
+}
+
+// The own row's 8 sub-block scales go to the scale table in one burst, after
+// the loop that computed them: no shared store sits between the loop's loads.
+__device__ __forceinline__ void store_scales(float* tab, const float (&scl)[8], int og, int orb, int ohi) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) tab[j * 32 + og * 4 + orb * 2 + ohi] = scl[j];
 }
 
 // Out of line: each phase function is entered once per phase, and its own
@@ -743,10 +750,10 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
       const uint4 hdr = *reinterpret_cast<const uint4*>(unit + 16 * lane);
       const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
       const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-      float* tab = reinterpret_cast<float*>(sm.stab(wc.warp, 0));
+      float scl[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        decode_step<NT>(j, hdr, d * row_unscale, dmin, tab, og, orb, ohi, sx + sbl * 8 * R, R, mtmp);
+      for (int j = 0; j < 8; ++j) scl[j] = decode_step<NT>(j, hdr, d * row_unscale, dmin, sx + sbl * 8 * R, R, mtmp);
+      store_scales(reinterpret_cast<float*>(sm.stab(wc.warp, 0)), scl, og, orb, ohi);
     }
 #pragma unroll
     for (int r = 0; r < 4 * NT; ++r) mn[r] = mtmp[r];
@@ -773,6 +780,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
       const uint8_t* codes = unit + kUnitHdr + lane * 16;
       const int boff = sbl * 512;
       const float* sxn = sx + sbl_next * 8 * R;
+      float scl[8];
 #pragma unroll
       for (int kp = 0; kp < 8; ++kp) {
         const uint4 w4 = *reinterpret_cast<const uint4*>(codes + kp * 512);
@@ -800,7 +808,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
         dequant_word(w4.w, av);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(t1[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
-        if (has_next) decode_step<NT>(kp, hdrn, dscalen, dminn, tabn, og, orb, ohi, sxn, R, mtmp);
+        scl[kp] = has_next ? decode_step<NT>(kp, hdrn, dscalen, dminn, sxn, R, mtmp) : 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           acc[0][nt][0] = fmaf(s4.x, t0[nt][0], acc[0][nt][0]);
@@ -813,6 +821,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
           acc[1][nt][3] = fmaf(s4.w, t1[nt][3], acc[1][nt][3]);
         }
       }
+      if (has_next) store_scales(tabn, scl, og, orb, ohi);
       release_unit(wc, sm);  // includes __syncwarp: both tables are settled
       if (++sbl == nsb_s || u + 1 == a.u1) {
         flush(tile, u + 1, reinterpret_cast<float*>(sm.stab(wc.warp, cur)));
