@@ -3,6 +3,8 @@
 // pending verify result), the page allocator (lowest free page first, in row
 // order; pages wholly beyond the committed length are freed), the per-step
 // descriptor and the single cooperative launch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -18,7 +20,7 @@
 namespace mk {
 cudaError_t pack_units(const PackSrc& p, uint8_t* dst, int n_tiles, int nsb, cudaStream_t s);
 cudaError_t launch_persistent(const ModelDesc* md, const StepDesc* sd, float* attn_scratch, int grid,
-                              cudaStream_t stream);
+                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, cudaStream_t stream);
 cudaError_t configure_persistent(int* blocks_per_sm);
 }  // namespace mk
 
@@ -164,6 +166,7 @@ struct mk_ctx {
   int32_t* out_host = nullptr;  // pinned [kOutInts + 4]
   int32_t* pt_host = nullptr;   // pinned page-table mirror
   float* attn_scratch = nullptr;
+  CUtensorMap tm_k{}, tm_v{};  // 2-D tensor maps of the K and V pools (attention page copies)
   std::vector<void*> allocs;
   std::vector<SeqInfo> seqs;
   std::set<int> free_pages;
@@ -286,6 +289,33 @@ void mk_free(mk_ctx* c) {
   delete c;
 }
 
+// 2-D tensor map over one KV pool: rows = (attention layer, page, kv head,
+// token), columns = the head's dh elements; boxes of 16 rows x box_w bytes.
+bool encode_kv_map(CUtensorMap* m, void* base, const mk_layout& L, int n_fa) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const int q8 = L.kv_dtype == MK_KV_Q8;
+  const AttnSlot S = attn_slot_layout(L.fa_dh, q8);
+  const int esz = q8 ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.fa_dh),
+                        static_cast<cuuint64_t>(n_fa) * L.n_pages * L.fa_hkv * L.page_tokens};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.fa_dh) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(S.box_w / esz), static_cast<cuuint32_t>(kChunk)};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(m, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                S.swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffers* b, void* stream,
                     mk_ctx** out) {
   if (!layout || !w || !b || !out) return MK_ERR_INVALID;
@@ -386,6 +416,10 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   auto gemm = [&](GemmDesc& g, const PhasePlan& ph, int pro, int epi, const float* gain) {
     g.w = packed + ph.off; g.n_tiles = ph.n_tiles; g.nsb = ph.nsb; g.n_out = ph.n_out;
     g.pro = pro; g.epi = epi; g.gain = gain;
+    g.zero_buf = ZERO_NONE;
+    g.img_in = (pro == PRO_RMS_X || pro == PRO_H) ? 1 : 0;
+    g.img_out = 0;
+    g.img_gain = nullptr;
     max_tiles = std::max(max_tiles, ph.n_tiles);
     max_seg = std::max(max_seg, max_segments(ph.n_tiles, ph.nsb, c->grid));
   };
@@ -403,25 +437,52 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
     ld.conv_w = gdn ? reinterpret_cast<const float*>(packed + p.off_conv[l]) : nullptr;
   }
   gemm(md.lm, p.lm, PRO_RMS_X, EPI_TOP2, reinterpret_cast<const float*>(packed + p.off_final_norm));
+  // split tiles are summed into buffers that must start at zero: the
+  // gate/up sums are cleared during o_proj, the next input projections during down
+  for (int l = 0; l < L.n_layers; ++l) {
+    md.layer[l].o.zero_buf = ZERO_GU;
+    md.layer[l].down.zero_buf = ZERO_YIN;
+  }
+  // image producers: o_proj -> gate/up (ffn norm), gate/up -> down (no norm),
+  // down -> next layer's input projections (attention norm) or lm_head
+  for (int l = 0; l < L.n_layers; ++l) {
+    LayerDesc& ld = md.layer[l];
+    ld.o.img_out = 1;
+    ld.o.img_gain = ld.gu.gain;
+    ld.gu.img_out = 1;
+    ld.gu.img_gain = nullptr;
+    ld.down.img_out = 1;
+    ld.down.img_gain = l + 1 < L.n_layers ? md.layer[l + 1].in.gain : md.lm.gain;
+  }
   md.final_norm = reinterpret_cast<const float*>(packed + p.off_final_norm);
   md.embed = packed + p.off_embed;
   md.max_seg = max_seg;
   md.kv_k = b->kv_k; md.kv_v = b->kv_v;
   md.kv_ks = static_cast<uint16_t*>(b->kv_k_scale); md.kv_vs = static_cast<uint16_t*>(b->kv_v_scale);
+  if (p.n_fa > 0 && (!encode_kv_map(&c->tm_k, b->kv_k, L, p.n_fa) || !encode_kv_map(&c->tm_v, b->kv_v, L, p.n_fa))) {
+    mk_free(c);
+    return MK_ERR_CUDA;
+  }
   md.gdn_state = b->gdn_state; md.conv_state = b->conv_state;
 
   const size_t nrec = static_cast<size_t>(c->grid) * kWarps;
   const size_t attn_items_max = static_cast<size_t>(2 * c->grid + kMaxSeqs * std::max(1, L.fa_hkv));
   c->tickets_bytes = static_cast<size_t>(max_tiles) * 4;
   c->attn_tickets_bytes = static_cast<size_t>(kMaxSeqs) * std::max(1, L.fa_hkv) * 4;
-  if ((e = dev_alloc(c, &md.x, static_cast<size_t>(kMaxRows) * H * 4)) ||
+  md.img_k = std::max(H, F);
+  if ((e = dev_alloc(c, &md.img_h[0], static_cast<size_t>(2 * kMaxRows) * md.img_k * 2)) ||
+      (e = dev_alloc(c, &md.img_h[1], static_cast<size_t>(2 * kMaxRows) * md.img_k * 2)) ||
+      (e = dev_alloc(c, &md.img_p[0], static_cast<size_t>(md.img_k / 16) * kMaxRows * 4)) ||
+      (e = dev_alloc(c, &md.img_p[1], static_cast<size_t>(md.img_k / 16) * kMaxRows * 4)) ||
+      (e = dev_alloc(c, &md.x, static_cast<size_t>(kMaxRows) * H * 4)) ||
       (e = dev_alloc(c, &md.xsq, static_cast<size_t>(H / 32) * kMaxRows * 4)) ||
       (e = dev_alloc(c, &md.yin, static_cast<size_t>(kMaxRows) * p.n_in_max * 4)) ||
       (e = dev_alloc(c, &md.o, static_cast<size_t>(kMaxRows) * std::max(1, p.o_stride) * 4)) ||
       (e = dev_alloc(c, &md.h, static_cast<size_t>(kMaxRows) * F * 4)) ||
-      (e = dev_alloc(c, &md.partial, nrec * max_seg * kMaxRows * 32 * 4)) ||
+      (e = dev_alloc(c, &md.gu, static_cast<size_t>(kMaxRows) * 2 * F * 4)) ||
+      (e = dev_alloc(c, &md.logits, static_cast<size_t>(kMaxRows) * L.vocab * 4)) ||
       (e = dev_alloc(c, &md.tickets, c->tickets_bytes)) ||
-      (e = dev_alloc(c, &md.attn_part, attn_items_max * kMaxQRows * (kMaxDh + 2) * 4)) ||
+      (e = dev_alloc(c, &md.attn_part, attn_items_max * kMaxQRows * kPartStride * 4)) ||
       (e = dev_alloc(c, &md.attn_tickets, c->attn_tickets_bytes)) ||
       (e = dev_alloc(c, &md.top_val, nrec * kMaxRows * 4)) ||
       (e = dev_alloc(c, &md.top_idx, nrec * kMaxRows * 4)) ||
@@ -630,12 +691,30 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
     sd.row_tok[r] = tokens[r];
     sd.row_pos[r] = positions[r];
   }
-  int total_tiles = 0;
-  for (int i = 0; i < n_seq; ++i) total_tiles += (c->seqs[sid[i]].len + 31) / 32;
+  // attention: 16-token chunks of the cached context cut into about one
+  // item per block, at most kMaxSplits parts per (sequence, kv head)
+  int total_chunks = 0, t_max = 1;
+  for (int i = 0; i < n_seq; ++i) {
+    total_chunks += (c->seqs[sid[i]].len + kChunk - 1) / kChunk;
+    t_max = std::max(t_max, T[i]);
+  }
   const int hkv = std::max(1, L.fa_hkv);
-  int tps = std::max(1, (total_tiles * hkv + c->grid - 1) / c->grid);
-  for (int i = 0; i < n_seq; ++i)  // at most kMaxSplits parts per (sequence, kv head)
-    tps = std::max(tps, ((c->seqs[sid[i]].len + 31) / 32 + kMaxSplits - 1) / kMaxSplits);
+  int cps = std::max(1, (total_chunks * hkv + c->grid - 1) / c->grid);
+  int max_chunks = 1;
+  for (int i = 0; i < n_seq; ++i) {
+    const int nc = (c->seqs[sid[i]].len + kChunk - 1) / kChunk;
+    max_chunks = std::max(max_chunks, nc);
+    cps = std::max(cps, (nc + kMaxSplits - 1) / kMaxSplits);
+  }
+  // per-sequence rounding can push the item count past the grid; grow the
+  // split until every item has a block of its own
+  auto n_items = [&](int cp) {
+    int n = 0;
+    for (int i = 0; i < n_seq; ++i)
+      n += hkv * std::max(1, ((c->seqs[sid[i]].len + kChunk - 1) / kChunk + cp - 1) / cp);
+    return n;
+  };
+  while (cps < max_chunks && n_items(cps) > c->grid) ++cps;
   int items = 0;
   for (int i = 0; i < n_seq; ++i) {
     const SeqInfo& s = c->seqs[sid[i]];
@@ -652,9 +731,9 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
       c->step_snap[i][t] = at;
       ++at;
     }
-    const int ntile = (s.len + 31) / 32;
-    sd.seq_tiles_per_split[i] = tps;
-    sd.seq_nsplit[i] = std::max(1, (ntile + tps - 1) / tps);
+    const int nchunk = (s.len + kChunk - 1) / kChunk;
+    sd.seq_chunks_per_split[i] = cps;
+    sd.seq_nsplit[i] = std::max(1, (nchunk + cps - 1) / cps);
     sd.seq_item0[i] = items;
     items += hkv * sd.seq_nsplit[i];
     for (int j = 0; j < T[i]; ++j) sd.row_si[row0[i] + j] = i;
@@ -662,6 +741,11 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
     c->step_T[i] = T[i];
   }
   sd.n_attn_items = items;
+  if (L.fa_dh > 0) {
+    attn_plan(t_max * (L.fa_hq / hkv), L.fa_dh, L.kv_dtype == MK_KV_Q8, kRingBytes, sd.attn_dsplit, sd.attn_wpg,
+              sd.attn_ng, sd.attn_spg, sd.attn_nslots);
+    if (sd.attn_spg < 1) return MK_ERR_UNSUPPORTED;
+  }
   sd.skip_block = c->skip_block;
   sd.skip_barrier = c->skip_barrier;
   sd.barrier_timeout_ns = c->barrier_timeout_ns;
@@ -690,7 +774,8 @@ mk_status mk_step_launch(mk_ctx* c) {
       cudaMemsetAsync(c->md_host.err, 0, 64, c->stream) != cudaSuccess)
     return MK_ERR_CUDA;
   cudaEventRecord(c->ev0, c->stream);
-  const cudaError_t e = launch_persistent(c->md_dev, c->sd_dev, c->attn_scratch, c->grid, c->stream);
+  const cudaError_t e =
+      launch_persistent(c->md_dev, c->sd_dev, c->attn_scratch, c->grid, &c->tm_k, &c->tm_v, c->stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? MK_ERR_LAUNCH : MK_ERR_CUDA;
@@ -770,7 +855,7 @@ constexpr int kMaxDevices = 64;
 void* g_static_addr[kMaxDevices] = {nullptr};
 
 struct StaticLayout {
-  size_t md, x, xsq, yin, o, h, partial, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
+  size_t md, img_h0, img_h1, img_p0, img_p1, x, xsq, yin, o, h, gu, logits, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
       attn_scratch, total;
 };
 
@@ -781,14 +866,19 @@ StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
   size_t at = 0;
   auto take = [&](size_t& off, size_t bytes) { off = at; at = align_up(at + (bytes ? bytes : 16)); };
   take(L.md, sizeof(ModelDesc));
+  take(L.img_h0, static_cast<size_t>(2 * kMaxRows) * md.img_k * 2);
+  take(L.img_h1, static_cast<size_t>(2 * kMaxRows) * md.img_k * 2);
+  take(L.img_p0, static_cast<size_t>(md.img_k / 16) * kMaxRows * 4);
+  take(L.img_p1, static_cast<size_t>(md.img_k / 16) * kMaxRows * 4);
   take(L.x, static_cast<size_t>(kMaxRows) * md.H * 4);
   take(L.xsq, static_cast<size_t>(md.H / 32) * kMaxRows * 4);
   take(L.yin, static_cast<size_t>(kMaxRows) * md.n_in_max * 4);
   take(L.o, static_cast<size_t>(kMaxRows) * std::max(1, md.o_stride) * 4);
   take(L.h, static_cast<size_t>(kMaxRows) * md.F * 4);
-  take(L.partial, nrec * md.max_seg * kMaxRows * 32 * 4);
+  take(L.gu, static_cast<size_t>(kMaxRows) * 2 * md.F * 4);
+  take(L.logits, static_cast<size_t>(kMaxRows) * md.V * 4);
   take(L.tickets, c->tickets_bytes);
-  take(L.attn_part, static_cast<size_t>(std::max(1, n_attn_items)) * kMaxQRows * (kMaxDh + 2) * 4);
+  take(L.attn_part, static_cast<size_t>(std::max(1, n_attn_items)) * kMaxQRows * kPartStride * 4);
   take(L.attn_tickets, c->attn_tickets_bytes);
   take(L.top_val, nrec * kMaxRows * 4);
   take(L.top_idx, nrec * kMaxRows * 4);
@@ -823,12 +913,17 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
   const StaticLayout SL = static_layout(c, c->sd_host->n_attn_items);
   uint8_t* base = static_cast<uint8_t*>(g_static_addr[dev]);
   ModelDesc md = c->md_host;
+  md.img_h[0] = reinterpret_cast<__half*>(base + SL.img_h0);
+  md.img_h[1] = reinterpret_cast<__half*>(base + SL.img_h1);
+  md.img_p[0] = reinterpret_cast<float*>(base + SL.img_p0);
+  md.img_p[1] = reinterpret_cast<float*>(base + SL.img_p1);
   md.x = reinterpret_cast<float*>(base + SL.x);
   md.xsq = reinterpret_cast<float*>(base + SL.xsq);
   md.yin = reinterpret_cast<float*>(base + SL.yin);
   md.o = reinterpret_cast<float*>(base + SL.o);
   md.h = reinterpret_cast<float*>(base + SL.h);
-  md.partial = reinterpret_cast<float*>(base + SL.partial);
+  md.gu = reinterpret_cast<float*>(base + SL.gu);
+  md.logits = reinterpret_cast<float*>(base + SL.logits);
   md.tickets = reinterpret_cast<uint32_t*>(base + SL.tickets);
   md.attn_part = reinterpret_cast<float*>(base + SL.attn_part);
   md.attn_tickets = reinterpret_cast<uint32_t*>(base + SL.attn_tickets);
@@ -847,7 +942,7 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
       cudaMemsetAsync(md.err, 0, 64, c->stream) != cudaSuccess ||
       cudaStreamSynchronize(c->stream) != cudaSuccess)
     return MK_ERR_CUDA;
-  const cudaError_t e = launch_persistent(md_dev, c->sd_dev, attn_scratch, c->grid, c->stream);
+  const cudaError_t e = launch_persistent(md_dev, c->sd_dev, attn_scratch, c->grid, &c->tm_k, &c->tm_v, c->stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? MK_ERR_LAUNCH : MK_ERR_CUDA;

@@ -4,6 +4,8 @@
 // of the library include it; nothing outside csrc/ does.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include <cstdint>
 
 #include "mk.h"
@@ -57,15 +59,27 @@ constexpr int kMaxSeqs = MK_MAX_SEQS;
 constexpr int kMaxDh = 256;
 constexpr int kMaxQRows = 48;                 // T x (hq/hkv) rows attending one kv head
 constexpr int kMaxSplits = 128;               // split-K parts of one (sequence, kv head)
+constexpr int kChunk = 16;                    // cached tokens per attention chunk (one KV page)
+constexpr int kPartStride = kMaxDh + 4;       // floats per query row of a split partial: dims, m, l, pad
+constexpr int kAttnMaxSlots = 16;             // KV staging slots (their mbarriers live in misc)
+constexpr int kAttnBarOff = 3840;             // byte offset of those mbarriers inside misc
 
 // ------------------------------------------------------------- descriptors
 enum Prologue : int32_t { PRO_RMS_X = 0, PRO_GDN_OUT = 1, PRO_FA_OUT = 2, PRO_H = 3 };
+enum ZeroBuf : int32_t { ZERO_NONE = 0, ZERO_GU = 1, ZERO_YIN = 2 };
 enum Epilogue : int32_t { EPI_STORE_YIN = 0, EPI_RESID_X = 1, EPI_SWIGLU_H = 2, EPI_TOP2 = 3 };
 
 struct GemmDesc {
   const uint8_t* w;  // units [n_tiles][nsb]
-  int32_t n_tiles, nsb, n_out, pro, epi, pad;
-  const float* gain; // RMSNorm gain (PRO_RMS_X) or per-head output-norm gain (PRO_GDN_OUT)
+  int32_t n_tiles, nsb, n_out, pro, epi;
+  int32_t img_in;    // 1: the activations come from the image the previous phase wrote
+  int32_t img_out;   // 1: the epilogue writes the next phase's activation image
+  int32_t pad;
+  const float* gain;      // RMSNorm gain (PRO_RMS_X) or per-head output-norm gain (PRO_GDN_OUT)
+  const float* img_gain;  // gain the written image is multiplied by (NULL: none)
+  // a buffer a later phase accumulates into, cleared (rows < R) at this phase's start
+  int32_t zero_buf;  // ZERO_NONE, ZERO_GU or ZERO_YIN
+  int32_t pad2;
 };
 
 struct LayerDesc {
@@ -91,14 +105,25 @@ struct ModelDesc {
   void* kv_k; void* kv_v; uint16_t* kv_ks; uint16_t* kv_vs;
   float* gdn_state; float* conv_state;
   // scratch
+  // Activation images, double-buffered by phase parity: the phase that
+  // produces a GEMM's input writes it once, already split into fp16 high/low
+  // columns in the permuted B-fragment order (img_h [2*kMaxRows][img_k]) with
+  // per-16 sums of (high+low) (img_p [img_k/16][R]); RMSNorm's 1/rms is left
+  // out and applied to the GEMM's output rows instead.
+  __half* img_h[2];
+  float* img_p[2];
+  int32_t img_k;
+  int32_t pad_img;
   float* x;          // [kMaxRows][H] residual stream
   float* xsq;        // [H/32][kMaxRows] sums of squares of x over each 32-wide chunk
   float* yin;        // [kMaxRows][n_in_max] input projections
   float* o;          // [kMaxRows][o_stride] mixer outputs
-  float* h;          // [kMaxRows][F] SwiGLU outputs
+  float* h;          // [kMaxRows][F] SwiGLU output
+  float* gu;         // [kMaxRows][2F] gate/up outputs of split tiles (summed by red.add)
+  float* logits;     // [kMaxRows][V] lm_head outputs of split tiles (summed by red.add)s
   float* partial;    // [grid*kWarps][max_seg][kMaxRows][32]
   uint32_t* tickets; // per tile
-  float* attn_part;  // [attn items][kMaxQRows][dh + 2]
+  float* attn_part;  // [attn items][kMaxQRows][kPartStride]: dims, then m and l (log2 units)
   uint32_t* attn_tickets;  // per (step sequence, kv head)
   float* top_val;    // [grid*kWarps][kMaxRows]
   int32_t* top_idx;  // [grid*kWarps][kMaxRows]
@@ -124,7 +149,9 @@ struct StepDesc {
   int32_t seq_id[kMaxSeqs], seq_row0[kMaxSeqs], seq_T[kMaxSeqs], seq_len[kMaxSeqs];
   int32_t seq_slot_in[kMaxSeqs], seq_snap_all[kMaxSeqs];
   int32_t seq_slot_out[kMaxSeqs][kMaxT];
-  int32_t seq_nsplit[kMaxSeqs], seq_tiles_per_split[kMaxSeqs], seq_item0[kMaxSeqs];
+  int32_t seq_nsplit[kMaxSeqs], seq_chunks_per_split[kMaxSeqs], seq_item0[kMaxSeqs];
+  // attention plan of this step (attn_plan): warp groups and KV staging slots
+  int32_t attn_dsplit, attn_wpg, attn_ng, attn_spg, attn_nslots;
   int32_t skip_block, skip_barrier;
   uint64_t barrier_timeout_ns;
   float2 rope[kMaxRows][kMaxDh / 2];  // (cos, sin) of position * base^(-2i/dh)
@@ -154,6 +181,53 @@ struct Sched {
 };
 
 __host__ __device__ inline int act_col_stride(int nsb_slice) { return nsb_slice * 512 + 64; }
+
+// ------------------------------------------------ attention KV staging
+// One slot holds one 16-token page of one kv head: K then V, each as boxes
+// of 16 rows x box_w bytes written by a 2-D tensor copy (128-byte rows with
+// the 128-byte swizzle: 16-byte chunk k of row t lands at chunk k ^ (t & 7);
+// q8 rows narrower than 128 bytes are unswizzled 64-byte boxes), then for q8
+// the K and V block scales of the page ([16][dh/32] binary16 each).
+struct AttnSlot {
+  int32_t box_w;      // bytes per box row (128, or 64 for unswizzled q8 boxes)
+  int32_t nbox;       // boxes per K (and per V)
+  int32_t swz;        // 1: 128-byte swizzle
+  int32_t v_off, ks_off, vs_off, bytes, tx_bytes;
+};
+
+__host__ __device__ inline AttnSlot attn_slot_layout(int dh, int q8) {
+  AttnSlot L;
+  const int row_bytes = q8 ? dh : 2 * dh;
+  L.swz = (row_bytes % 128 == 0) ? 1 : 0;
+  L.box_w = L.swz ? 128 : 64;
+  L.nbox = row_bytes / L.box_w;
+  const int kv = L.nbox * kChunk * L.box_w;  // bytes of K (or V) codes
+  L.v_off = kv;
+  L.ks_off = 2 * kv;
+  L.vs_off = 2 * kv + (q8 ? kChunk * (dh / 32) * 2 : 0);
+  const int end = L.vs_off + (q8 ? kChunk * (dh / 32) * 2 : 0);
+  L.bytes = (end + 1023) / 1024 * 1024;
+  L.tx_bytes = end;
+  return L;
+}
+
+// Warp groups of the attention phase. A warp owns one n-tile of 8 query rows
+// (of the T x hq/hkv rows attending one kv head) and 1/dsplit of the head
+// dimension; the wpg warps covering all n-tiles form a group that consumes
+// one chunk at a time; ng groups take a CTA item's chunks round-robin.
+__host__ __device__ inline void attn_plan(int q_rows_max, int dh, int q8, int ring_bytes, int32_t& dsplit,
+                                          int32_t& wpg, int32_t& ng, int32_t& spg, int32_t& nslots) {
+  const int nq = (q_rows_max + 7) / 8;
+  dsplit = (nq <= 2 && (dh / 16) % 2 == 0) ? 2 : 1;
+  wpg = nq * dsplit;
+  ng = kWarps / wpg;
+  if (ng < 1) ng = 1;
+  const AttnSlot L = attn_slot_layout(dh, q8);
+  nslots = (ring_bytes - 1024) / L.bytes;  // room for aligning the first slot to 1024 bytes
+  if (nslots > kAttnMaxSlots) nslots = kAttnMaxSlots;
+  spg = nslots / ng;
+  nslots = spg * ng;
+}
 
 __host__ __device__ inline int act_bytes(int nsb_slice, int R) {
   return 2 * R * act_col_stride(nsb_slice) + nsb_slice * 8 * R * 4;  // = 1056 R n + 128 R

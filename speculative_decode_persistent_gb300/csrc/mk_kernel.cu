@@ -24,6 +24,7 @@
 // 32-wide sub-block's two mma sums are scaled in fp32 by d * sc_j * 2^24 (or
 // 2^20), and the min term dmin * sum_j m_j * sum(x over sub-block j) is added
 // by the lane that owns the weight row. Weights are used exactly as stored.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -135,23 +136,27 @@ __device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + expf
 __device__ __forceinline__ float siluf_(float v) { return v / (1.0f + expf(-v)); }
 
 // --------------------------------------------------------- shared memory
+// The block's dynamic shared memory. Every region is addressed from this
+// array directly, so the compiler keeps shared-window (32-bit) addressing in
+// every phase function.
+extern __shared__ __align__(128) uint8_t smem_raw[];
+
 struct Smem {
-  uint8_t* base;
   __device__ uint8_t* ring(int warp, int slot) const {
-    return base + kOffRing + (warp * kRing + slot) * kUnitBytes;
+    return smem_raw + kOffRing + (warp * kRing + slot) * kUnitBytes;
   }
   __device__ uint64_t* bar(int warp, int slot) const {  // full: the unit has landed
-    return reinterpret_cast<uint64_t*>(base + kOffBar) + warp * kRing + slot;
+    return reinterpret_cast<uint64_t*>(smem_raw + kOffBar) + warp * kRing + slot;
   }
   __device__ uint64_t* empty(int warp, int slot) const {  // the math warp is done with the slot
-    return reinterpret_cast<uint64_t*>(base + kOffBar) + kWarps * kRing + warp * kRing + slot;
+    return reinterpret_cast<uint64_t*>(smem_raw + kOffBar) + kWarps * kRing + warp * kRing + slot;
   }
   __device__ uint32_t* stab(int warp, int buf) const {
-    return reinterpret_cast<uint32_t*>(base + kOffTab + (warp * 2 + buf) * kWarpTab);
+    return reinterpret_cast<uint32_t*>(smem_raw + kOffTab + (warp * 2 + buf) * kWarpTab);
   }
-  __device__ uint8_t* act() const { return base + kOffAct; }
-  __device__ float* misc() const { return reinterpret_cast<float*>(base + kOffMisc); }
-  __device__ uint8_t* phase() const { return base + kOffPhase; }
+  __device__ uint8_t* act() const { return smem_raw + kOffAct; }
+  __device__ float* misc() const { return reinterpret_cast<float*>(smem_raw + kOffMisc); }
+  __device__ uint8_t* phase() const { return smem_raw + kOffPhase; }
 };
 
 // -------------------------------------------------------------- grid sync
@@ -202,7 +207,8 @@ __device__ bool grid_sync(const ModelDesc& md, const StepDesc& sd, int& nbar, in
 // wait on the slot's "full" barrier and release it through its "empty" one.
 struct WarpCtx {
   int warp, lane, gid;
-  uint32_t c_pos;  // units consumed by this math warp
+  uint32_t c_pos;   // units consumed by this math warp
+  uint32_t kv_pos;  // attention chunks consumed by this warp's group
 };
 
 __device__ __forceinline__ const GemmDesc& gemm_desc(const ModelDesc& md, int gp) {
@@ -263,66 +269,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Lanes 0..kWarps-1 each walk one math warp's unit sequence; the warp stays
-// converged: every sweep, each lane issues its next unit if that unit's slot
-// has been released, then the sweep repeats until every lane is done.
-__device__ void producer_warp(const ModelDesc& md, const StepDesc& sd, const Smem& sm) {
-  const int lane = threadIdx.x & 31;
-  const int w = lane < kWarps ? lane : 0;
-  const uint64_t pol = evict_first_policy();
-  int gp = -1;
-  uint32_t left = 0, tile = 0, sbl = 0, p = 0;
-  int nsb_s = 1, sb0 = 0, nsb = 1;
-  const uint8_t* wsrc = nullptr;
-  bool done = lane >= kWarps;
-  volatile int32_t* err = md.err;
-  uint64_t t_idle = 0;
-  for (uint32_t sweep = 0;; ++sweep) {
-    // advance to the next phase with units for this lane's warp
-    while (!done && left == 0) {
-      if (++gp > 4 * md.n_layers) { done = true; break; }
-      const GemmDesc& g = gemm_desc(md, gp);
-      const Assign a = assign_for(g, sd.R, gridDim.x, blockIdx.x, w);
-      left = a.u1 - a.u0;
-      nsb_s = a.nsb_s;
-      tile = a.u0 / nsb_s;
-      sbl = a.u0 - tile * nsb_s;
-      sb0 = a.sb0;
-      nsb = g.nsb;
-      wsrc = g.w;
-    }
-    if (__all_sync(0xffffffffu, done)) break;
-    bool issued = false;
-    if (!done) {
-      const int slot = p % kRing;
-      if (mbar_test(sm.empty(w, slot), ((p / kRing) & 1u) ^ 1u)) {
-        uint64_t* b = sm.bar(w, slot);
-        mbar_arrive_expect_tx(b, kUnitBytes);
-        bulk_g2s(sm.ring(w, slot), wsrc + (static_cast<size_t>(tile) * nsb + sb0 + sbl) * kUnitBytes, kUnitBytes,
-                 b, pol);
-        if (++sbl == static_cast<uint32_t>(nsb_s)) { sbl = 0; ++tile; }
-        --left;
-        ++p;
-        issued = true;
-      }
-    }
-    if (__any_sync(0xffffffffu, issued)) {
-      t_idle = 0;
-    } else if ((sweep & 63u) == 63u) {
-      // nothing could be issued: the math warps are behind; give up only on
-      // an error or after the deadline
-      if (*err != 0) break;
-      const uint64_t now = globaltimer();
-      if (t_idle == 0) t_idle = now;
-      else if (now - t_idle > sd.barrier_timeout_ns) { atomicCAS(md.err, 0, DEV_COPY_TIMEOUT); break; }
-    }
-  }
-  // the block must not exit while a copy into its shared memory is in flight
-  if (lane < kWarps)
-    for (uint32_t q = p > static_cast<uint32_t>(kRing) ? p - kRing : 0; q < p; ++q)
-      mbar_wait_bounded(sm.bar(w, q % kRing), (q / kRing) & 1u, md, 50000000ull, DEV_COPY_TIMEOUT);
-}
-
 __device__ __forceinline__ bool wait_unit(const WarpCtx& wc, const Smem& sm, const ModelDesc& md,
                                           uint64_t timeout_ns) {
   return mbar_wait_bounded(sm.bar(wc.warp, wc.c_pos % kRing), (wc.c_pos / kRing) & 1u, md, timeout_ns,
@@ -338,6 +284,14 @@ __device__ __forceinline__ void release_unit(WarpCtx& wc, const Smem& sm) {
 
 // ------------------------------------------------------------------ embed
 __device__ void embed_phase(const ModelDesc& md, const StepDesc& sd, const WarpCtx& wc) {
+  // the step's accumulation buffers start at zero: first input projections,
+  // first gate/up, lm_head
+  {
+    const int stride = gridDim.x * kThreads, t0 = blockIdx.x * kThreads + threadIdx.x;
+    for (int idx = t0; idx < sd.R * md.n_in_max; idx += stride) md.yin[idx] = 0.f;
+    for (int idx = t0; idx < sd.R * 2 * md.F; idx += stride) md.gu[idx] = 0.f;
+    for (int idx = t0; idx < sd.R * md.V; idx += stride) md.logits[idx] = 0.f;
+  }
   const int nsbH = md.H / 256;
   const int total = sd.R * nsbH;
   for (int it = wc.gid; it < total; it += gridDim.x * kWarps) {
@@ -424,7 +378,7 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
   __half* act = reinterpret_cast<__half*>(sm.act());
   float* sx = reinterpret_cast<float*>(sm.act() + 2 * R * cstride);
   float* misc = sm.misc();                        // 1/rms per row
-  float* red = misc + 1024 - kWarps * kMaxRows;   // [warp][row] partial sums
+  float* red = misc + 512;                        // [warp][row] partial sums
   const int per_row = ks / 4;
   const int cs2 = cstride / 2;
   const int total = R * per_row;
@@ -503,13 +457,7 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
   math_sync();
 }
 
-// ------------------------------------------------------------- top-2 state
-template <int NR>
-struct Top2 {
-  float b1[NR];
-  int i1[NR];
-};
-
+// ------------------------------------------------------------- top-1 state
 // Larger value wins; on an exact tie the lower vocabulary index wins.
 __device__ __forceinline__ void top1_merge(float& a1, int& ai, float b1, int bi) {
   if (b1 > a1 || (b1 == a1 && bi < ai)) {
@@ -518,16 +466,29 @@ __device__ __forceinline__ void top1_merge(float& a1, int& ai, float b1, int bi)
   }
 }
 
+// Running top-1 of every row over the lm_head tiles a warp has finished:
+// kMaxRows (value, index) pairs per warp in the misc region.
+constexpr int kTopRecOff = 640;  // float offset inside misc
+static_assert((kTopRecOff + kWarps * 2 * kMaxRows) * 4 <= kAttnBarOff, "top-1 records");
+__device__ __forceinline__ float* top_rec(int warp) {
+  return reinterpret_cast<float*>(smem_raw + kOffMisc) + kTopRecOff + warp * 2 * kMaxRows;
+}
+
 // --------------------------------------------------------- GEMM epilogue
+// v[r] is the complete output of the lane's row n = 32 tile + lane for
+// activation row r. For a tile that several warps computed, the outputs were
+// summed in global memory (red.add into the phase's output buffer) and v was
+// read back from there: `summed` marks that case (then x already holds the
+// residual sum and yin needs nothing more).
 template <int NT, bool TOP>
 __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g,
-                                              uint32_t tile, const float (&v)[4 * NT], int lane,
-                                              Top2<4 * NT>& top) {
+                                              uint32_t tile, const float (&v)[4 * NT], int lane, int warp,
+                                              bool summed) {
   const int R = sd.R;
   const int n = static_cast<int>(tile) * kTileRows + lane;
   switch (g.epi) {
     case EPI_STORE_YIN:
-      if (n < g.n_out) {
+      if (!summed && n < g.n_out) {
 #pragma unroll
         for (int r = 0; r < 4 * NT; ++r)
           if (r < R) md.yin[static_cast<size_t>(r) * md.n_in_max + n] = v[r];
@@ -539,8 +500,11 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
       for (int r = 0; r < 4 * NT; ++r)
         if (r < R) {
           float* p = md.x + static_cast<size_t>(r) * md.H + n;
-          const float xn = __ldcg(p) + v[r];
-          *p = xn;
+          float xn = v[r];
+          if (!summed) {
+            xn += __ldcg(p);
+            *p = xn;
+          }
           const float sq = warp_sum(xn * xn);  // the next RMSNorm's partial for this 32-wide chunk
           if (lane == 0) md.xsq[static_cast<size_t>(tile) * kMaxRows + r] = sq;
         }
@@ -557,15 +521,34 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
       break;
     }
     case EPI_TOP2:
-      if (TOP && n < md.V) {
+      if (TOP) {
+        float* rec = top_rec(warp);
 #pragma unroll
         for (int r = 0; r < 4 * NT; ++r)
           if (r < R) {
-            const float x = v[r];
-            if (!isfinite(x)) atomicOr(&md.err[1], 1);
-            top1_merge(top.b1[r], top.i1[r], x, n);
-            if (md.dbg_logits) md.dbg_logits[static_cast<size_t>(r) * md.V + n] = x;
+            float x = -FLT_MAX;
+            int ix = 0x7fffffff;
+            if (n < md.V) {
+              x = v[r];
+              ix = n;
+              if (!isfinite(x)) atomicOr(&md.err[1], 1);
+              if (md.dbg_logits) md.dbg_logits[static_cast<size_t>(r) * md.V + n] = x;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const float ox = __shfl_xor_sync(0xffffffffu, x, o);
+              const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
+              top1_merge(x, ix, ox, oi);
+            }
+            if (lane == 0) {
+              float b = rec[2 * r];
+              int bi = __float_as_int(rec[2 * r + 1]);
+              top1_merge(b, bi, x, ix);
+              rec[2 * r] = b;
+              rec[2 * r + 1] = __int_as_float(bi);
+            }
           }
+        __syncwarp();
       }
       break;
   }
@@ -632,6 +615,11 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
   const int R = sd.R;
   const int grid = gridDim.x;
   const Assign a = assign_for(g, R, grid, blockIdx.x, wc.warp);
+  if (g.zero_buf != ZERO_NONE) {  // a later phase's accumulation buffer starts at zero
+    float* zp = g.zero_buf == ZERO_GU ? md.gu : md.yin;
+    const int cols = g.zero_buf == ZERO_GU ? 2 * md.F : md.n_in_max;
+    for (int idx = blockIdx.x * kThreads + threadIdx.x; idx < R * cols; idx += grid * kThreads) zp[idx] = 0.f;
+  }
   gemm_prologue(md, sd, g, a.sb0, a.nsb_s, sm);
 
   const int lane = wc.lane, gq = lane >> 2, cq = lane & 3;
@@ -648,11 +636,17 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
   const uint8_t* bcol[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) bcol[nt] = act + min(nt * 8 + gq, 2 * R - 1) * cstride + cq * 16;
-
-  Top2<4 * NT> top;
+  // where split tiles are summed
+  float* dst = g.epi == EPI_STORE_YIN ? md.yin : g.epi == EPI_RESID_X ? md.x : g.epi == EPI_SWIGLU_H ? md.gu : md.logits;
+  const int dstride = g.epi == EPI_STORE_YIN ? md.n_in_max : g.epi == EPI_RESID_X ? md.H
+                      : g.epi == EPI_SWIGLU_H ? 2 * md.F : md.V;
   if (TOP) {
-#pragma unroll
-    for (int r = 0; r < 4 * NT; ++r) { top.b1[r] = -FLT_MAX; top.i1[r] = 0x7fffffff; }
+    float* rec = top_rec(wc.warp);
+    if (lane < R) {
+      rec[2 * lane] = -FLT_MAX;
+      rec[2 * lane + 1] = __int_as_float(0x7fffffff);
+    }
+    __syncwarp();
   }
 
   float acc[2][NT][4];
@@ -673,67 +667,50 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
       for (int nt = 0; nt < NT; ++nt) {
         const int r = nt * 4 + cq;
         if (r < R) {
-          stage[(rb * 16 + gq) * 16 + r] = acc[rb][nt][0] + acc[rb][nt][1];
-          stage[(rb * 16 + gq + 8) * 16 + r] = acc[rb][nt][2] + acc[rb][nt][3];
+          stage[(rb * 16 + gq) * 17 + r] = acc[rb][nt][0] + acc[rb][nt][1];
+          stage[(rb * 16 + gq + 8) * 17 + r] = acc[rb][nt][2] + acc[rb][nt][3];
         }
       }
     __syncwarp();
     float v[4 * NT];
 #pragma unroll
-    for (int r = 0; r < 4 * NT; ++r) v[r] = r < R ? stage[lane * 16 + r] - mn[r] : 0.f;
+    for (int r = 0; r < 4 * NT; ++r) v[r] = r < R ? stage[lane * 17 + r] - mn[r] : 0.f;
     __syncwarp();
     const uint32_t tu0 = tile * nsb_s, tu1 = tu0 + nsb_s;
-    const bool complete = a.sc.S == 1 && seg_u0 == tu0 && u_end == tu1;
-    if (!complete) {
-      const int seg_idx = static_cast<int>(tile - a.u0 / nsb_s);
-      float* slot = md.partial + (static_cast<size_t>(wc.gid) * md.max_seg + seg_idx) * kMaxRows * 32;
+    if (a.sc.S == 1 && seg_u0 == tu0 && u_end == tu1) {  // the whole tile: no one else contributes
+      gemm_epilogue<NT, TOP>(md, sd, g, tile, v, lane, wc.warp, false);
+      return;
+    }
+    const int n = static_cast<int>(tile) * kTileRows + lane;
+    if (n < g.n_out) {
 #pragma unroll
       for (int r = 0; r < 4 * NT; ++r)
-        if (r < R) __stcg(slot + r * 32 + lane, v[r]);
-      __threadfence();
-      __syncwarp();
-      uint32_t last = 0;
-      if (lane == 0) {
-        uint32_t n = 0;
-        for (int sl = 0; sl < a.sc.S; ++sl) {
-          const uint32_t ns = slice_nsb(a.sc, g.nsb, sl);
-          const uint32_t Us = static_cast<uint32_t>(g.n_tiles) * ns;
-          const uint32_t Ws =
-              static_cast<uint32_t>(slice_cta0(a.sc, grid, sl + 1) - slice_cta0(a.sc, grid, sl)) * kWarps;
-          n += segments_in(Us, Ws, tile * ns, tile * ns + ns);
-        }
-        const uint32_t old = atomicAdd(&md.tickets[tile], 1u);
-        last = (old + 1u == n) ? 1u : 0u;
-        if (last) md.tickets[tile] = 0u;
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (!last) return;
-      __threadfence();
-#pragma unroll
-      for (int r = 0; r < 4 * NT; ++r) v[r] = 0.f;
+        if (r < R) atomicAdd(dst + static_cast<size_t>(r) * dstride + n, v[r]);
+    }
+    if (g.epi == EPI_STORE_YIN) return;  // the sum itself is the output
+    __threadfence();
+    __syncwarp();
+    uint32_t last = 0;
+    if (lane == 0) {
+      uint32_t na = 0;
       for (int sl = 0; sl < a.sc.S; ++sl) {
         const uint32_t ns = slice_nsb(a.sc, g.nsb, sl);
-        const int c0 = slice_cta0(a.sc, grid, sl);
         const uint32_t Us = static_cast<uint32_t>(g.n_tiles) * ns;
-        const uint32_t Ws = static_cast<uint32_t>(slice_cta0(a.sc, grid, sl + 1) - c0) * kWarps;
-        const uint32_t ua = tile * ns, ub = ua + ns;
-        // warps holding units [ua, ub), in order: one per unit when ranges
-        // hold at most one unit, else the consecutive run wf..wl
-        const bool sparse = Us < Ws;
-        const uint32_t first = sparse ? ua : warp_of_unit(Us, Ws, ua);
-        const uint32_t last_w = sparse ? ub - 1 : warp_of_unit(Us, Ws, ub - 1);
-        for (uint32_t it = first; it <= last_w; ++it) {
-          const uint32_t ws = sparse ? warp_of_unit(Us, Ws, it) : it;
-          const int gid2 = (c0 + static_cast<int>(ws / kWarps)) * kWarps + static_cast<int>(ws % kWarps);
-          const int seg2 = static_cast<int>(tile - warp_u0(Us, Ws, ws) / ns);
-          const float* s2 = md.partial + (static_cast<size_t>(gid2) * md.max_seg + seg2) * kMaxRows * 32;
-#pragma unroll
-          for (int r = 0; r < 4 * NT; ++r)
-            if (r < R) v[r] += __ldcg(s2 + r * 32 + lane);
-        }
+        const uint32_t Ws =
+            static_cast<uint32_t>(slice_cta0(a.sc, grid, sl + 1) - slice_cta0(a.sc, grid, sl)) * kWarps;
+        na += segments_in(Us, Ws, tile * ns, tile * ns + ns);
       }
+      const uint32_t old = atomicAdd(&md.tickets[tile], 1u);
+      last = (old + 1u == na) ? 1u : 0u;
+      if (last) md.tickets[tile] = 0u;
     }
-    gemm_epilogue<NT, TOP>(md, sd, g, tile, v, lane, top);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+#pragma unroll
+    for (int r = 0; r < 4 * NT; ++r)
+      v[r] = (r < R && n < g.n_out) ? __ldcg(dst + static_cast<size_t>(r) * dstride + n) : 0.f;
+    gemm_epilogue<NT, TOP>(md, sd, g, tile, v, lane, wc.warp, true);
   };
 
   bool ok = true;
@@ -790,36 +767,48 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           bf[nt] = *reinterpret_cast<const uint4*>(bcol[nt] + boff + kp * 64);
-        float t0[NT][4], t1[NT][4];  // sub-block sums of halves 0 and 1 (two k-steps each)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) t0[nt][e] = t1[nt][e] = 0.f;
         uint32_t av[4];
-        dequant_word(w4.x, av);
+        {  // rows 0..15 of the tile: words x (k-step 0) and z (k-step 1)
+          float t[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(t0[nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
-        dequant_word(w4.y, av);
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(t1[nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
-        dequant_word(w4.z, av);
+            for (int e = 0; e < 4; ++e) t[nt][e] = 0.f;
+          dequant_word(w4.x, av);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(t0[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
-        dequant_word(w4.w, av);
+          for (int nt = 0; nt < NT; ++nt) mma16816(t[nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
+          dequant_word(w4.z, av);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(t1[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
-        scl[kp] = has_next ? decode_step<NT>(kp, hdrn, dscalen, dminn, sxn, R, mtmp) : 0.f;
+          for (int nt = 0; nt < NT; ++nt) mma16816(t[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          acc[0][nt][0] = fmaf(s4.x, t0[nt][0], acc[0][nt][0]);
-          acc[0][nt][1] = fmaf(s4.x, t0[nt][1], acc[0][nt][1]);
-          acc[0][nt][2] = fmaf(s4.y, t0[nt][2], acc[0][nt][2]);
-          acc[0][nt][3] = fmaf(s4.y, t0[nt][3], acc[0][nt][3]);
-          acc[1][nt][0] = fmaf(s4.z, t1[nt][0], acc[1][nt][0]);
-          acc[1][nt][1] = fmaf(s4.z, t1[nt][1], acc[1][nt][1]);
-          acc[1][nt][2] = fmaf(s4.w, t1[nt][2], acc[1][nt][2]);
-          acc[1][nt][3] = fmaf(s4.w, t1[nt][3], acc[1][nt][3]);
+          for (int nt = 0; nt < NT; ++nt) {
+            acc[0][nt][0] = fmaf(s4.x, t[nt][0], acc[0][nt][0]);
+            acc[0][nt][1] = fmaf(s4.x, t[nt][1], acc[0][nt][1]);
+            acc[0][nt][2] = fmaf(s4.y, t[nt][2], acc[0][nt][2]);
+            acc[0][nt][3] = fmaf(s4.y, t[nt][3], acc[0][nt][3]);
+          }
         }
+        {  // rows 16..31: words y and w
+          float t[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) t[nt][e] = 0.f;
+          dequant_word(w4.y, av);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816(t[nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
+          dequant_word(w4.w, av);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816(t[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            acc[1][nt][0] = fmaf(s4.z, t[nt][0], acc[1][nt][0]);
+            acc[1][nt][1] = fmaf(s4.z, t[nt][1], acc[1][nt][1]);
+            acc[1][nt][2] = fmaf(s4.w, t[nt][2], acc[1][nt][2]);
+            acc[1][nt][3] = fmaf(s4.w, t[nt][3], acc[1][nt][3]);
+          }
+        }
+        scl[kp] = has_next ? decode_step<NT>(kp, hdrn, dscalen, dminn, sxn, R, mtmp) : 0.f;
       }
       if (has_next) store_scales(tabn, scl, og, orb, ohi);
       release_unit(wc, sm);  // includes __syncwarp: both tables are settled
@@ -842,23 +831,10 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
     }
   }
 
-  if (TOP) {
-    // warp-level merge, then one record per warp
-#pragma unroll
-    for (int r = 0; r < 4 * NT; ++r) {
-      float b1 = top.b1[r];
-      int i1 = top.i1[r];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ob1 = __shfl_xor_sync(0xffffffffu, b1, o);
-        const int oi1 = __shfl_xor_sync(0xffffffffu, i1, o);
-        top1_merge(b1, i1, ob1, oi1);
-      }
-      if (lane == 0 && r < R) {
-        md.top_val[static_cast<size_t>(wc.gid) * kMaxRows + r] = b1;
-        md.top_idx[static_cast<size_t>(wc.gid) * kMaxRows + r] = i1;
-      }
-    }
+  if (TOP && lane < R) {  // one record per warp and row
+    const float* rec = top_rec(wc.warp);
+    md.top_val[static_cast<size_t>(wc.gid) * kMaxRows + lane] = rec[2 * lane];
+    md.top_idx[static_cast<size_t>(wc.gid) * kMaxRows + lane] = __float_as_int(rec[2 * lane + 1]);
   }
   return ok;
 }
@@ -1041,21 +1017,341 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
 // and values, then attends to them with the causal mask across the draft
 // rows. Splits write (m, l, acc) partials; the last block to finish a
 // (sequence, head) combines them in split order.
-struct AttnSmem {
-  __half* Q;   // [48][dh+8]
-  __half* K;   // [32][dh+8]
-  __half* V;   // [32][dh+8]
-  float* S;    // [48][33]
-  __half* P;   // [48][40]
-  float* m;    // [48]
-  float* l;    // [48]
-  float* sc;   // [48]
-  int* flag;
+// ---------------------------------------------------------------- attention
+// Split-K flash decoding over the paged KV pool, transposed so that the head
+// dimension and the tokens are the mma's M and K: per 16-token chunk a warp
+// forms S^T = K Q^T (16 tokens x 8 query rows), updates the online softmax of
+// its 8 query rows, and accumulates O^T += V^T P^T (its share of the head
+// dims x 8 rows) in registers. Pages arrive by tensor copies issued by the
+// producer warp into staging slots (the weight ring, idle during attention);
+// the warps of a group consume one chunk each time without block barriers.
+// The step's own rows form one more chunk (causal), built by the last split.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// Two bytes of x = w ^ 0x80808080 (selected by sel) -> the binary16 pair of
+// the original signed bytes, exactly: (byte + 128) becomes the mantissa of
+// 1024.0, then 1152.0 is subtracted.
+__device__ __forceinline__ uint32_t s8x2_to_h2(uint32_t x, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x64646464u), "r"(sel));
+  const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&r), __half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+  return h2u(h);
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// Byte offset, inside one K (or V) box set of a slot, of byte b of token t.
+__device__ __forceinline__ int kv_off(const AttnSlot& L, int t, int b) {
+  const int bx = b / L.box_w, bb = b - bx * L.box_w;
+  const int base = bx * kChunk * L.box_w + t * L.box_w;
+  return L.swz ? base + ((((bb >> 4) ^ (t & 7)) << 4) | (bb & 15)) : base + bb;
+}
+
+struct AttnBuf {
+  uint8_t* slots;   // first slot, 1024-byte aligned inside the ring region
+  uint64_t* full;   // [kAttnMaxSlots]: the chunk has landed
+  uint64_t* empty;  // [kAttnMaxSlots]: every warp of the group is done with it
 };
 
-__device__ void attn_store_kv(const ModelDesc& md, int fa_i, int page, int kh, int slot, const float* x,
-                              int which, __half* tile_row, int lane) {
-  // one warp, dh values in x (global scratch), writes the pool and the f16 tile row
+__device__ __forceinline__ AttnBuf attn_buf(const Smem& sm) {
+  AttnBuf b;
+  const uint32_t a = smem_u32(smem_raw + kOffRing);
+  b.slots = smem_raw + kOffRing + ((1024u - (a & 1023u)) & 1023u);
+  b.full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sm.misc()) + kAttnBarOff);
+  b.empty = b.full + kAttnMaxSlots;
+  return b;
+}
+
+struct AttnItem {
+  int si, kh, j, nsplit, cb, nch;
+};
+
+// Item = (sequence, kv head, split); split j covers chunks [cb, cb + nch).
+__device__ __forceinline__ AttnItem attn_item(const StepDesc& sd, int hkv, int item) {
+  AttnItem it;
+  int si = 0;
+  while (si + 1 < sd.n_seq && item >= sd.seq_item0[si + 1]) ++si;
+  const int local = item - sd.seq_item0[si];
+  it.si = si;
+  it.nsplit = sd.seq_nsplit[si];
+  it.kh = local / it.nsplit;
+  it.j = local % it.nsplit;
+  const int nchunk = (sd.seq_len[si] + kChunk - 1) / kChunk;
+  const int cps = sd.seq_chunks_per_split[si];
+  it.cb = it.j * cps;
+  it.nch = max(0, min(nchunk, it.cb + cps) - it.cb);
+  return it;
+}
+
+// Producer side: lane tg < ng walks group tg's chunks of this block's items
+// (chunk i of an item belongs to group i % ng) and copies each page (K and V
+// boxes, and the q8 scales) into the group's next slot once it is free; then
+// waits until the consumers have released every chunk. kv_issued counts the
+// lane's chunks over the whole step (it keys the slots' mbarrier phases).
+__device__ bool attn_stream(const ModelDesc& md, const StepDesc& sd, const Smem& sm, int layer,
+                            const CUtensorMap* tmk, const CUtensorMap* tmv, uint32_t& kv_issued, uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  const int ng = sd.attn_ng, spg = sd.attn_spg;
+  const AttnBuf ab = attn_buf(sm);
+  const AttnSlot SL = attn_slot_layout(md.dh, md.kv_q8);
+  const int fa_i = md.layer[layer].fa_i;
+  const int hkv = md.hkv;
+  const int bw = SL.box_w / (md.kv_q8 ? 1 : 2);  // box width in elements
+  const bool mine = lane < ng;
+  int item = blockIdx.x, i = lane;
+  AttnItem it{};
+  bool done = !mine;
+  auto seek = [&]() {
+    while (!done) {
+      if (item >= sd.n_attn_items) { done = true; break; }
+      it = attn_item(sd, hkv, item);
+      if (i < it.nch) break;
+      item += gridDim.x;
+      i = lane;
+    }
+  };
+  seek();
+  volatile int32_t* err = md.err;
+  uint64_t t_idle = 0;
+  bool ok = true;
+  for (uint32_t sweep = 0;; ++sweep) {
+    if (__all_sync(0xffffffffu, done)) break;
+    bool issued = false;
+    if (!done) {
+      const int slot = lane * spg + static_cast<int>(kv_issued % static_cast<uint32_t>(spg));
+      if (mbar_test(ab.empty + slot, ((kv_issued / spg) & 1u) ^ 1u)) {
+        const int page = md.page_table[static_cast<size_t>(sd.seq_id[it.si]) * md.max_pages_per_seq + it.cb + i];
+        const int row = ((fa_i * md.n_pages + page) * hkv + it.kh) * kChunk;
+        uint8_t* dst = ab.slots + slot * SL.bytes;
+        uint64_t* fb = ab.full + slot;
+        mbar_arrive_expect_tx(fb, SL.tx_bytes);
+        for (int bx = 0; bx < SL.nbox; ++bx) {
+          tma_load_2d(dst + bx * kChunk * SL.box_w, tmk, bx * bw, row, fb, pol);
+          tma_load_2d(dst + SL.v_off + bx * kChunk * SL.box_w, tmv, bx * bw, row, fb, pol);
+        }
+        if (md.kv_q8) {
+          const int sb = kChunk * (md.dh / 32) * 2;
+          bulk_g2s(dst + SL.ks_off, md.kv_ks + static_cast<size_t>(row) * (md.dh / 32), sb, fb, pol);
+          bulk_g2s(dst + SL.vs_off, md.kv_vs + static_cast<size_t>(row) * (md.dh / 32), sb, fb, pol);
+        }
+        ++kv_issued;
+        i += ng;
+        seek();
+        issued = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, issued)) {
+      t_idle = 0;
+    } else if ((sweep & 63u) == 63u) {
+      if (*err != 0) { ok = false; break; }
+      const uint64_t now = globaltimer();
+      if (t_idle == 0) t_idle = now;
+      else if (now - t_idle > sd.barrier_timeout_ns) { atomicCAS(md.err, 0, DEV_COPY_TIMEOUT); ok = false; break; }
+    }
+  }
+  if (ok && mine && kv_issued > 0) {
+    const uint32_t q = kv_issued - 1;
+    ok = mbar_wait_bounded(ab.empty + lane * spg + q % spg, (q / spg) & 1u, md, sd.barrier_timeout_ns,
+                           DEV_COPY_TIMEOUT);
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
+struct AttnState {
+  float m[2], l[2];             // running max and sum of query columns 2c, 2c+1
+  float acc[kMaxDh / 16][4];    // O^T: m-tile (16 dims) x (dim rows g, g+8) x (columns 2c, 2c+1)
+};
+
+// One chunk for one warp: K rows at kb, V rows at vb (slot layout), q8 block
+// scales at ks / vs. Tokens >= nvalid are masked; causal_grp > 0 also masks
+// token t for query row q when t > q / causal_grp (the step's own rows).
+// Scores are in log2 units (Q carries log2(e) / sqrt(dh)). SWZ: 128-byte
+// swizzled boxes (always for fp16; q8 when dh is a multiple of 128).
+template <bool Q8, bool SWZ>
+__device__ __forceinline__ void attn_chunk(const uint8_t* kb, const uint8_t* vb, const __half* ks, const __half* vs,
+                                           const __half* Qp, int qstride, int dh, int nt, int mt0, int nmt,
+                                           int nvalid, int causal_grp, int lane, AttnState& st) {
+  constexpr int BW = SWZ ? 128 : 64;  // bytes per box row
+  constexpr int BB = kChunk * BW;     // bytes per box
+  const int g = lane >> 2, c = lane & 3;
+  const int nblk = dh / 32;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd j chains
+  const __half* qa = Qp + (nt * 8 + (lane & 7)) * qstride + 8 * (lane >> 3);
+  if (!Q8) {
+    // lane c reads the 16-byte chunks 2c and 2c+1 of its box rows in turn
+    const uint8_t* kr0 = kb + g * 128 + (((2 * c) ^ g) << 4);
+    const uint8_t* kr1 = kb + g * 128 + (((2 * c + 1) ^ g) << 4);
+#pragma unroll 4
+    for (int j = 0; j < kMaxDh / 32; ++j) {
+      if (j < nblk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(b0, b1, b2, b3, qa + 32 * j);
+        const uint8_t* kr = ((j & 1) ? kr1 : kr0) + (j >> 1) * BB;
+        const uint4 x = *reinterpret_cast<const uint4*>(kr);
+        const uint4 y = *reinterpret_cast<const uint4*>(kr + 8 * 128);
+        float(&sj)[4] = (j & 1) ? s1 : s0;
+        mma16816(sj, x.x, y.x, x.y, y.y, b0, b1);
+        mma16816(sj, x.z, y.z, x.w, y.w, b2, b3);
+      }
+    }
+  } else {
+#pragma unroll 4
+    for (int j = 0; j < kMaxDh / 32; ++j) {
+      if (j < nblk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(b0, b1, b2, b3, qa + 32 * j);
+        const int byte = 32 * j + 8 * c;
+        int off;
+        if (SWZ) {
+          const int bb = byte & 127;
+          off = (byte >> 7) * BB + g * 128 + ((((bb >> 4) ^ g) << 4) | (bb & 15));
+        } else {
+          off = g * 64 + byte;
+        }
+        const uint2 x = *reinterpret_cast<const uint2*>(kb + off);
+        const uint2 y = *reinterpret_cast<const uint2*>(kb + off + 8 * BW);
+        const uint32_t xx = x.x ^ 0x80808080u, xy = x.y ^ 0x80808080u;
+        const uint32_t yx = y.x ^ 0x80808080u, yy = y.y ^ 0x80808080u;
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(t, s8x2_to_h2(xx, 0x4140u), s8x2_to_h2(yx, 0x4140u), s8x2_to_h2(xx, 0x4342u),
+                 s8x2_to_h2(yx, 0x4342u), b0, b1);
+        mma16816(t, s8x2_to_h2(xy, 0x4140u), s8x2_to_h2(yy, 0x4140u), s8x2_to_h2(xy, 0x4342u),
+                 s8x2_to_h2(yy, 0x4342u), b2, b3);
+        const float sg = __half2float(ks[g * nblk + j]), sg8 = __half2float(ks[(g + 8) * nblk + j]);
+        float(&sj)[4] = (j & 1) ? s1 : s0;
+        sj[0] = fmaf(sg, t[0], sj[0]);
+        sj[1] = fmaf(sg, t[1], sj[1]);
+        sj[2] = fmaf(sg8, t[2], sj[2]);
+        sj[3] = fmaf(sg8, t[3], sj[3]);
+      }
+    }
+  }
+  float sc[4] = {s0[0] + s1[0], s0[1] + s1[1], s0[2] + s1[2], s0[3] + s1[3]};
+  // masks: rows g / g+8 are tokens, columns q0 / q0+1 are query rows
+  const int q0 = nt * 8 + 2 * c;
+  bool v0 = g < nvalid, v1 = v0, v2 = g + 8 < nvalid, v3 = v2;
+  if (causal_grp > 0) {
+    v0 = v0 && g <= q0 / causal_grp;
+    v1 = v1 && g <= (q0 + 1) / causal_grp;
+    v2 = v2 && g + 8 <= q0 / causal_grp;
+    v3 = v3 && g + 8 <= (q0 + 1) / causal_grp;
+  }
+  sc[0] = v0 ? sc[0] : -INFINITY;
+  sc[1] = v1 ? sc[1] : -INFINITY;
+  sc[2] = v2 ? sc[2] : -INFINITY;
+  sc[3] = v3 ? sc[3] : -INFINITY;
+  float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+  float a0 = 1.f, a1 = 1.f, p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+  if (mn0 != -INFINITY) {
+    a0 = exp2f(st.m[0] - mn0);
+    p0 = exp2f(sc[0] - mn0);
+    p2 = exp2f(sc[2] - mn0);
+  }
+  if (mn1 != -INFINITY) {
+    a1 = exp2f(st.m[1] - mn1);
+    p1 = exp2f(sc[1] - mn1);
+    p3 = exp2f(sc[3] - mn1);
+  }
+  float r0 = p0 + p2, r1 = p1 + p3;
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    r0 += __shfl_xor_sync(0xffffffffu, r0, o);
+    r1 += __shfl_xor_sync(0xffffffffu, r1, o);
+  }
+  st.l[0] = fmaf(st.l[0], a0, r0);
+  st.l[1] = fmaf(st.l[1], a1, r1);
+  st.m[0] = mn0;
+  st.m[1] = mn1;
+#pragma unroll
+  for (int mi = 0; mi < kMaxDh / 16; ++mi) {
+    st.acc[mi][0] *= a0;
+    st.acc[mi][1] *= a1;
+    st.acc[mi][2] *= a0;
+    st.acc[mi][3] *= a1;
+  }
+  // O^T += V^T P^T: A = V^T from the V rows (ldmatrix.trans), B = P^T from
+  // the S^T accumulators transposed per 8x8 block
+  const int vt = (lane & 7) + 8 * (lane >> 4);  // token row this lane addresses
+  const int vsub = (lane >> 3) & 1;
+  const uint8_t* vrow = vb + vt * BW;
+  if (!Q8) {
+    const uint32_t pb0 = movm_trans(h2u(__floats2half2_rn(p0, p1)));
+    const uint32_t pb1 = movm_trans(h2u(__floats2half2_rn(p2, p3)));
+    // tokens 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3) beyond nvalid hold no data
+    const uint32_t mlo = (2 * c < nvalid ? 0xffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
+    const uint32_t mhi = (2 * c + 8 < nvalid ? 0xffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int mi = 0; mi < kMaxDh / 16; ++mi) {
+      if (mi < nmt) {
+        const int M = mt0 + mi;  // 16 dims = 32 bytes: box M / 4, chunks 2 (M % 4) + vsub
+        const uint8_t* addr = vrow + (M >> 2) * BB + (((2 * (M & 3) + vsub) ^ (lane & 7)) << 4);
+        uint32_t x0, x1, x2, x3;
+        ldsm_x4_trans(x0, x1, x2, x3, addr);
+        mma16816(st.acc[mi], x0 & mlo, x1 & mlo, x2 & mhi, x3 & mhi, pb0, pb1);
+      }
+    }
+  } else {
+    // V = scale[token][block] x code: the scale goes into P^T per block
+#pragma unroll
+    for (int jb = 0; jb < kMaxDh / 32; ++jb) {
+      if (2 * jb < nmt) {
+        const int blk = mt0 / 2 + jb;
+        const float sg = g < nvalid ? __half2float(vs[g * nblk + blk]) : 0.f;
+        const float sg8 = g + 8 < nvalid ? __half2float(vs[(g + 8) * nblk + blk]) : 0.f;
+        const uint32_t pb0 = movm_trans(h2u(__floats2half2_rn(p0 * sg, p1 * sg)));
+        const uint32_t pb1 = movm_trans(h2u(__floats2half2_rn(p2 * sg8, p3 * sg8)));
+        const uint8_t* addr = SWZ ? vrow + (blk >> 2) * BB + (((2 * (blk & 3) + vsub) ^ (lane & 7)) << 4)
+                                  : vrow + 32 * blk + 16 * vsub;
+        uint32_t r0_, r1_, r2_, r3_;
+        ldsm_x4_trans(r0_, r1_, r2_, r3_, addr);
+        r0_ ^= 0x80808080u;
+        r1_ ^= 0x80808080u;
+        r2_ ^= 0x80808080u;
+        r3_ ^= 0x80808080u;
+        // m-rows g / g+8 of a tile are the block's even / odd dims
+        mma16816(st.acc[2 * jb], s8x2_to_h2(r0_, 0x4240u), s8x2_to_h2(r0_, 0x4341u), s8x2_to_h2(r2_, 0x4240u),
+                 s8x2_to_h2(r2_, 0x4341u), pb0, pb1);
+        mma16816(st.acc[2 * jb + 1], s8x2_to_h2(r1_, 0x4240u), s8x2_to_h2(r1_, 0x4341u),
+                 s8x2_to_h2(r3_, 0x4240u), s8x2_to_h2(r3_, 0x4341u), pb0, pb1);
+      }
+    }
+  }
+}
+
+// Head dim held by accumulator row `row` (0..15) of m-tile M.
+template <bool Q8>
+__device__ __forceinline__ int attn_dim(int M, int row) {
+  if (!Q8) return M * 16 + row;
+  return (M >> 1) * 32 + (M & 1) * 16 + (row < 8 ? 2 * row : 2 * (row - 8) + 1);
+}
+
+// One row of the step's own K or V: rounded (fp16 pool) or quantised (q8
+// pool) into the pool, and the same stored values into the new-rows chunk.
+__device__ void attn_store_kv(const ModelDesc& md, int fa_i, int page, int kh, int slot, const float* x, int which,
+                              uint8_t* tile, __half* tile_scales, const AttnSlot& SL, int t, int lane) {
   const int dh = md.dh;
   const size_t row = ((static_cast<size_t>(fa_i) * md.n_pages + page) * md.hkv + kh) * md.page_tokens + slot;
   if (!md.kv_q8) {
@@ -1063,7 +1359,7 @@ __device__ void attn_store_kv(const ModelDesc& md, int fa_i, int page, int kh, i
     for (int d = lane; d < dh; d += 32) {
       const __half hv = __float2half_rn(x[d]);
       dst[d] = hv;
-      tile_row[d] = hv;
+      *reinterpret_cast<__half*>(tile + kv_off(SL, t, 2 * d)) = hv;
     }
   } else {
     int8_t* codes = reinterpret_cast<int8_t*>(which ? md.kv_v : md.kv_k) + row * dh;
@@ -1080,360 +1376,287 @@ __device__ void attn_store_kv(const ModelDesc& md, int fa_i, int page, int kh, i
         q = static_cast<int>(qq);
       }
       codes[32 * b + lane] = static_cast<int8_t>(q);
-      if (lane == 0) scales[b] = __half_as_ushort(d16);
-      tile_row[32 * b + lane] = __float2half_rn(__half2float(d16) * static_cast<float>(q));
+      tile[kv_off(SL, t, 32 * b + lane)] = static_cast<uint8_t>(static_cast<int8_t>(q));
+      if (lane == 0) {
+        scales[b] = __half_as_ushort(d16);
+        tile_scales[t * (dh / 32) + b] = d16;
+      }
     }
   }
 }
 
-__device__ __noinline__ void attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const Smem& sm, float* scratch_row) {
+// Shared memory of the attention phase, inside the phase region.
+constexpr int kAttnQBytes = (kMaxQRows * (kMaxDh + 8) * 2 + 255) / 256 * 256;
+constexpr int kAttnNewBytes = 16384;                          // largest slot (fp16, dh 256)
+constexpr int kAttnMergeBytes = 4 * (4 + 4 * (kMaxDh / 16)) * 32 * 4;  // worst plan: 1 x 4 warps, 16 m-tiles
+static_assert(kAttnQBytes + kAttnNewBytes + kAttnMergeBytes + 16 <= kPhaseBytes, "attention shared memory");
+static_assert(kWarps * kMaxSplits * 4 <= kAttnMergeBytes, "attention combine weights");
+static_assert(kAttnBarOff + 2 * kAttnMaxSlots * 8 <= kMiscBytes, "attention mbarriers");
+
+// The last block of a (sequence, kv head) merges the splits' partials with
+// all its math threads: split weights 2^(m_s - M) per query row into shared
+// memory, then one thread per (query row, 4 head dims) sums the splits with
+// 16-byte loads, several in flight.
+__device__ __noinline__ void attn_combine(const ModelDesc& md, const StepDesc& sd, int si, int kh, int nsplit,
+                                          int qrows, int row0, float* wsm) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int dh = md.dh, grp = md.hq / md.hkv;
+  __threadfence();
+  const int item0 = sd.seq_item0[si] + kh * nsplit;
+  float* wm = wsm;                    // [qrows][nsplit]: m, then the weight
+  float* inv = wsm + qrows * nsplit;  // [qrows]
+  auto part = [&](int sp, int r) {
+    return md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + r) * kPartStride;
+  };
+  for (int idx = tid; idx < qrows * nsplit; idx += kThreads) wm[idx] = __ldcg(part(idx % nsplit, idx / nsplit) + kMaxDh);
+  math_sync();
+  for (int r = warp; r < qrows; r += kWarps) {
+    float mloc = -INFINITY;
+    for (int sp = lane; sp < nsplit; sp += 32) mloc = fmaxf(mloc, wm[r * nsplit + sp]);
+    const float M = warp_max(mloc);
+    float lloc = 0.f;
+    for (int sp = lane; sp < nsplit; sp += 32) {
+      const float ms = wm[r * nsplit + sp];
+      const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      wm[r * nsplit + sp] = w;
+      lloc = fmaf(__ldcg(part(sp, r) + kMaxDh + 1), w, lloc);
+    }
+    const float tot = warp_sum(lloc);
+    if (lane == 0) inv[r] = 1.0f / tot;
+  }
+  math_sync();
+  const int d4n = dh / 4;
+  for (int idx = tid; idx < qrows * d4n; idx += kThreads) {
+    const int r = idx / d4n, d4 = idx - r * d4n;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(part(sp, r)) + d4);
+      const float w = wm[r * nsplit + sp];
+      a.x = fmaf(w, v.x, a.x);
+      a.y = fmaf(w, v.y, a.y);
+      a.z = fmaf(w, v.z, a.z);
+      a.w = fmaf(w, v.w, a.w);
+    }
+    const float iv = inv[r];
+    const int t = r / grp, hh = kh * grp + r % grp;
+    float4* o = reinterpret_cast<float4*>(md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh) + d4;
+    *o = make_float4(a.x * iv, a.y * iv, a.z * iv, a.w * iv);
+  }
+}
+
+template <bool Q8, bool SWZ>
+__device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const Smem& sm,
+                                        float* scratch_row, WarpCtx& wc) {
   const LayerDesc& L = md.layer[layer];
   const int fa_i = L.fa_i;
   const int dh = md.dh, hkv = md.hkv, grp = md.hq / md.hkv;
-  const int dpad = dh + 8;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, cq = lane & 3;
-  uint8_t* base = sm.phase();
-  AttnSmem as;
-  as.Q = reinterpret_cast<__half*>(base);
-  as.K = as.Q + kMaxQRows * dpad;
-  as.V = as.K + 32 * dpad;
-  as.S = reinterpret_cast<float*>(as.V + 32 * dpad);
-  as.P = reinterpret_cast<__half*>(as.S + kMaxQRows * 33);
-  as.m = reinterpret_cast<float*>(as.P + kMaxQRows * 40);
-  as.l = as.m + kMaxQRows;
-  as.sc = as.l + kMaxQRows;
-  as.flag = reinterpret_cast<int*>(as.sc + kMaxQRows);
-  float* wbuf = reinterpret_cast<float*>(as.flag + 4);  // [kWarps][kMaxSplits] split weights
-  const float inv_sqrt_dh = 1.0f / sqrtf(static_cast<float>(dh));
-  const int kq_off = 2 * md.hq * dh;           // k after q and gate
-  const int vq_off = kq_off + hkv * dh;         // v after k
+  const int tid = threadIdx.x, warp = wc.warp, lane = wc.lane;
+  const int g = lane >> 2, c = lane & 3;
+  const AttnSlot SL = attn_slot_layout(dh, Q8 ? 1 : 0);
+  const AttnBuf ab = attn_buf(sm);
+  const int ng = sd.attn_ng, wpg = sd.attn_wpg, dsplit = sd.attn_dsplit, spg = sd.attn_spg;
+  const int tg = warp / wpg, wi = warp % wpg;
+  const bool in_group = tg < ng;
+  const int nt = wi / dsplit, dp = wi % dsplit;
+  const int nmt = (dh / 16) / dsplit, mt0 = dp * nmt;
+  const int qstride = dh + 8;
+  __half* Qp = reinterpret_cast<__half*>(sm.phase());
+  uint8_t* newt = sm.phase() + kAttnQBytes;
+  float* mbuf = reinterpret_cast<float*>(sm.phase() + kAttnQBytes + kAttnNewBytes);
+  int* flag = reinterpret_cast<int*>(sm.phase() + kAttnQBytes + kAttnNewBytes + kAttnMergeBytes);
+  const float q_scale = 1.4426950408889634f / sqrtf(static_cast<float>(dh));  // log2(e) / sqrt(dh)
+  const int kq_off = 2 * md.hq * dh;    // k after q and gate
+  const int vq_off = kq_off + hkv * dh;  // v after k
+  const int mstride = 4 + 4 * nmt;      // floats per lane of one warp's merge record
+  bool ok = true;
 
   for (int item = blockIdx.x; item < sd.n_attn_items; item += gridDim.x) {
-    int si = 0;
-    while (si + 1 < sd.n_seq && item >= sd.seq_item0[si + 1]) ++si;
-    const int local = item - sd.seq_item0[si];
-    const int nsplit = sd.seq_nsplit[si];
-    const int kh = local / nsplit, j = local % nsplit;
+    const AttnItem it = attn_item(sd, hkv, item);
+    const int si = it.si, kh = it.kh;
     const int seq = sd.seq_id[si], T = sd.seq_T[si], row0 = sd.seq_row0[si], Lc = sd.seq_len[si];
-    const int qrows = T * grp, mt = (qrows + 15) / 16;
-    const int ntile = (Lc + 31) / 32;
-    const int tps = sd.seq_tiles_per_split[si];
-    const int tb = j * tps, te = min(ntile, tb + tps);
-    const bool last = j == nsplit - 1;
+    const int qrows = T * grp, nq = (qrows + 7) / 8;
+    const bool last = it.j == it.nsplit - 1;
     const int* pt = md.page_table + static_cast<size_t>(seq) * md.max_pages_per_seq;
 
-    // Q: RoPE, 1/sqrt(dh), fp16; padding rows zero
-    for (int idx = tid; idx < mt * 16 * (dh / 2); idx += kThreads) {
-      const int qr = idx / (dh / 2), i = idx % (dh / 2);
-      __half qa = __float2half_rn(0.f), qb = qa;
+    // Q (RoPE, 1/sqrt(dh), binary16), head dims in the order the K fragments
+    // present them; rows past qrows are zero
+    for (int idx = tid; idx < nq * 8 * (dh / 2); idx += kThreads) {
+      const int qr = idx / (dh / 2), pp = 2 * (idx % (dh / 2));
+      const int sidx = pp >> 4, l16 = pp & 15, j = sidx >> 1, h = sidx & 1, cc = (l16 & 7) >> 1, hi = l16 >> 3;
+      const int d = Q8 ? 32 * j + 8 * cc + 4 * h + 2 * hi : 64 * (j >> 1) + 16 * cc + 8 * (j & 1) + 4 * h + 2 * hi;
+      float v0 = 0.f, v1 = 0.f;
       if (qr < qrows) {
         const int t = qr / grp, hh = kh * grp + qr % grp, row = row0 + t;
         const float* q = md.yin + static_cast<size_t>(row) * md.n_in_max + hh * dh;
-        const float a = __ldcg(q + i), b = __ldcg(q + i + dh / 2);
-        const float2 cs = sd.rope[row][i];
-        qa = __float2half_rn((a * cs.x - b * cs.y) * inv_sqrt_dh);
-        qb = __float2half_rn((a * cs.y + b * cs.x) * inv_sqrt_dh);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int dd = d + e, i = dd % (dh / 2);
+          const float a = __ldcg(q + i), b = __ldcg(q + i + dh / 2);
+          const float2 cs = sd.rope[row][i];
+          const float v = (dd < dh / 2 ? a * cs.x - b * cs.y : a * cs.y + b * cs.x) * q_scale;
+          if (e == 0) v0 = v; else v1 = v;
+        }
       }
-      as.Q[qr * dpad + i] = qa;
-      as.Q[qr * dpad + i + dh / 2] = qb;
+      *reinterpret_cast<__half2*>(Qp + qr * qstride + pp) = __floats2half2_rn(v0, v1);
     }
-    for (int qr = tid; qr < kMaxQRows; qr += kThreads) {
-      as.m[qr] = -INFINITY;
-      as.l[qr] = 0.f;
+    // the step's own rows (last split): RoPE k, store K/V into the pool, and
+    // keep the stored values as one more chunk, causal over the T rows
+    if (last) {
+      for (int idx = tid; idx < SL.tx_bytes / 16; idx += kThreads)
+        reinterpret_cast<uint4*>(newt)[idx] = make_uint4(0u, 0u, 0u, 0u);
+      math_sync();
+      for (int t = warp; t < T; t += kWarps) {
+        const int row = row0 + t, pos = Lc + t;
+        const int page = pt[pos / md.page_tokens], slot = pos % md.page_tokens;
+        const float* kr = md.yin + static_cast<size_t>(row) * md.n_in_max + kq_off + kh * dh;
+        const float* vr = md.yin + static_cast<size_t>(row) * md.n_in_max + vq_off + kh * dh;
+        float* ksr = scratch_row + warp * 2 * kMaxDh;  // per-warp staging in global scratch
+        float* vsr = ksr + kMaxDh;
+        for (int i = lane; i < dh / 2; i += 32) {
+          const float a = __ldcg(kr + i), b = __ldcg(kr + i + dh / 2);
+          const float2 cs = sd.rope[row][i];
+          ksr[i] = a * cs.x - b * cs.y;
+          ksr[i + dh / 2] = a * cs.y + b * cs.x;
+        }
+        for (int d = lane; d < dh; d += 32) vsr[d] = __ldcg(vr + d);
+        __syncwarp();
+        attn_store_kv(md, fa_i, page, kh, slot, ksr, 0, newt, reinterpret_cast<__half*>(newt + SL.ks_off), SL, t,
+                      lane);
+        attn_store_kv(md, fa_i, page, kh, slot, vsr, 1, newt + SL.v_off, reinterpret_cast<__half*>(newt + SL.vs_off),
+                      SL, t, lane);
+        __syncwarp();
+      }
     }
-    const int nd = dh / kWarps;     // dims per warp in P V
-    const int nn = nd / 8;          // n-tiles per warp
-    float acc[3][4][4];
-#pragma unroll
-    for (int a = 0; a < 3; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
     math_sync();
 
-    const int n_iter = (te - tb) + (last ? 1 : 0);
-    // K/V tile staging: each thread holds up to 8 raw 16-byte (fp16) or
-    // 8-byte (q8, plus its block scale) vectors of the NEXT cached tile in
-    // registers, so the tile's load latency overlaps the current tile's work.
-    const int vec_per_row = dh / 8;
-    const int nvec = 2 * 32 * vec_per_row;  // K and V rows of 32 tokens
-    uint4 pf[8];
-    uint16_t pfs[8];
-    auto load_tile = [&](int tile) {
+    AttnState st;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
 #pragma unroll
-      for (int jv = 0; jv < 8; ++jv) {
-        const int idx = tid + jv * kThreads;
-        pf[jv] = make_uint4(0u, 0u, 0u, 0u);
-        pfs[jv] = 0;
-        if (idx < nvec) {
-          const int which = idx / (32 * vec_per_row);
-          const int rem = idx % (32 * vec_per_row);
-          const int tk = rem / vec_per_row, vi = rem % vec_per_row;
-          const int tok = tile * 32 + tk;
-          if (tok < Lc) {
-            const int page = pt[tok / md.page_tokens], slot = tok % md.page_tokens;
-            const size_t row = ((static_cast<size_t>(fa_i) * md.n_pages + page) * hkv + kh) * md.page_tokens + slot;
-            if (!md.kv_q8) {
-              pf[jv] = __ldcg(reinterpret_cast<const uint4*>(
-                  reinterpret_cast<const __half*>(which ? md.kv_v : md.kv_k) + row * dh + vi * 8));
-            } else {
-              const uint2 c8 = __ldcg(reinterpret_cast<const uint2*>(
-                  reinterpret_cast<const int8_t*>(which ? md.kv_v : md.kv_k) + row * dh + vi * 8));
-              pf[jv].x = c8.x;
-              pf[jv].y = c8.y;
-              pfs[jv] = __ldcg((which ? md.kv_vs : md.kv_ks) + row * (dh / 32) + (vi * 8) / 32);
-            }
-          }
-        }
-      }
-    };
-    auto store_tile = [&]() {
+    for (int mi = 0; mi < kMaxDh / 16; ++mi)
 #pragma unroll
-      for (int jv = 0; jv < 8; ++jv) {
-        const int idx = tid + jv * kThreads;
-        if (idx < nvec) {
-          const int which = idx / (32 * vec_per_row);
-          const int rem = idx % (32 * vec_per_row);
-          const int tk = rem / vec_per_row, vi = rem % vec_per_row;
-          __half* dst = (which ? as.V : as.K) + tk * dpad + vi * 8;
-          uint4 val = pf[jv];
-          if (md.kv_q8) {
-            // masked tokens stay zero: their codes and scale were never loaded
-            const float d16 = __half2float(__ushort_as_half(pfs[jv]));
-            const int8_t* cb = reinterpret_cast<const int8_t*>(&pf[jv]);
-            __half hv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) hv[e] = __float2half_rn(d16 * static_cast<float>(cb[e]));
-            val = *reinterpret_cast<uint4*>(hv);
-          }
-          *reinterpret_cast<uint4*>(dst) = val;
+      for (int e = 0; e < 4; ++e) st.acc[mi][e] = 0.f;
+    const bool active = in_group && nt < nq;
+    // this block's chunks round-robin over the groups; the step's own rows
+    // (last split) are one more chunk, read from the new-rows tile
+    if (in_group) {
+      const int nv = it.nch + (last ? 1 : 0);
+      for (int i = tg; i < nv; i += ng) {
+        const bool cached = i < it.nch;
+        const int slot = tg * spg + static_cast<int>(wc.kv_pos % static_cast<uint32_t>(spg));
+        const uint8_t* cb = newt;
+        int nvalid = T, causal = grp;
+        if (cached) {
+          if (ok)
+            ok = mbar_wait_bounded(ab.full + slot, (wc.kv_pos / spg) & 1u, md, sd.barrier_timeout_ns,
+                                   DEV_COPY_TIMEOUT);
+          cb = ab.slots + slot * SL.bytes;
+          nvalid = min(kChunk, Lc - (it.cb + i) * kChunk);
+          causal = 0;
         }
-      }
-    };
-    if (te > tb) load_tile(tb);
-    for (int it = 0; it < n_iter; ++it) {
-      const bool newtile = last && it == n_iter - 1;
-      const int tile = tb + it;
-      // ---- K/V tile (32 tokens) as fp16
-      if (!newtile) {
-        store_tile();
-        if (tile + 1 < te) load_tile(tile + 1);
-      } else {
-        // this step's own keys/values: RoPE k, round or quantise, append, keep as the tile
-        for (int idx = tid; idx < 32 * dh; idx += kThreads) {
-          const int tk = idx / dh, d = idx % dh;
-          if (tk >= T) {
-            as.K[tk * dpad + d] = __float2half_rn(0.f);
-            as.V[tk * dpad + d] = __float2half_rn(0.f);
-          }
-        }
-        for (int t = warp; t < T; t += kWarps) {
-          const int row = row0 + t, pos = Lc + t;
-          const int page = pt[pos / md.page_tokens], slot = pos % md.page_tokens;
-          const float* kr = md.yin + static_cast<size_t>(row) * md.n_in_max + kq_off + kh * dh;
-          const float* vr = md.yin + static_cast<size_t>(row) * md.n_in_max + vq_off + kh * dh;
-          float* ks = scratch_row + warp * 2 * kMaxDh;  // per-warp staging in global scratch
-          float* vs = ks + kMaxDh;
-          for (int i = lane; i < dh / 2; i += 32) {
-            const float a = __ldcg(kr + i), b = __ldcg(kr + i + dh / 2);
-            const float2 cs = sd.rope[row][i];
-            ks[i] = a * cs.x - b * cs.y;
-            ks[i + dh / 2] = a * cs.y + b * cs.x;
-          }
-          for (int d = lane; d < dh; d += 32) vs[d] = __ldcg(vr + d);
+        if (ok && active)
+          attn_chunk<Q8, SWZ>(cb, cb + SL.v_off, reinterpret_cast<const __half*>(cb + SL.ks_off),
+                              reinterpret_cast<const __half*>(cb + SL.vs_off), Qp, qstride, dh, nt, mt0, nmt, nvalid,
+                              causal, lane, st);
+        if (cached) {
           __syncwarp();
-          attn_store_kv(md, fa_i, page, kh, slot, ks, 0, as.K + t * dpad, lane);
-          attn_store_kv(md, fa_i, page, kh, slot, vs, 1, as.V + t * dpad, lane);
-          __syncwarp();
+          if (lane == 0) mbar_arrive(ab.empty + slot);
+          ++wc.kv_pos;
         }
       }
-      math_sync();
-      // ---- S = Q K^T (scaled already)
-      for (int unit = warp; unit < mt * 4; unit += kWarps) {
-        const int mi = unit / 4, ni = unit % 4;
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k16 = 0; k16 < dh / 16; ++k16) {
-          uint32_t a0, a1, a2, a3, b0, b1;
-          const int ar = mi * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int ac = k16 * 16 + (lane >> 4) * 8;
-          ldsm_x4(a0, a1, a2, a3, as.Q + ar * dpad + ac);
-          const int br = ni * 8 + (lane & 7);
-          const int bc = k16 * 16 + ((lane >> 3) & 1) * 8;
-          ldsm_x2(b0, b1, as.K + br * dpad + bc);
-          mma16816(s4, a0, a1, a2, a3, b0, b1);
-        }
-        const int r0 = mi * 16 + gq, c0 = ni * 8 + 2 * cq;
-        as.S[r0 * 33 + c0] = s4[0];
-        as.S[r0 * 33 + c0 + 1] = s4[1];
-        as.S[(r0 + 8) * 33 + c0] = s4[2];
-        as.S[(r0 + 8) * 33 + c0 + 1] = s4[3];
+    }
+
+    // merge the groups into group 0, in group order
+    if (ng > 1) {
+      if (in_group && tg > 0) {
+        float* pb = mbuf + ((tg - 1) * wpg + wi) * mstride * 32 + lane;
+        pb[0] = st.m[0];
+        pb[32] = st.m[1];
+        pb[64] = st.l[0];
+        pb[96] = st.l[1];
+#pragma unroll
+        for (int mi = 0; mi < kMaxDh / 16; ++mi)
+          if (mi < nmt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pb[(4 + 4 * mi + e) * 32] = st.acc[mi][e];
       }
       math_sync();
-      // ---- online softmax, one row per warp iteration, lane = token
-      for (int qr = warp; qr < mt * 16; qr += kWarps) {
-        float p = 0.f, scl = 1.f;
-        if (qr < qrows) {
-          const int t = qr / grp;
-          bool valid;
-          if (!newtile) valid = tile * 32 + lane < Lc;
-          else valid = lane <= t;
-          const float s = valid ? as.S[qr * 33 + lane] : -INFINITY;
-          const float mx = warp_max(s);
-          const float m_old = as.m[qr];
-          const float m_new = fmaxf(m_old, mx);
-          if (m_new == -INFINITY) {
-            p = 0.f;
-            scl = 1.f;
-          } else {
-            p = valid ? expf(s - m_new) : 0.f;
-            scl = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
-          }
-          const float sum = warp_sum(p);
-          if (lane == 0) {
-            as.l[qr] = as.l[qr] * scl + sum;
-            as.m[qr] = m_new;
-          }
-        }
-        as.P[qr * 40 + lane] = __float2half_rn(p);
-        if (lane == 0) as.sc[qr] = scl;
-      }
-      math_sync();
-      // ---- acc = acc * scale + P V  (warp w owns dims [w*nd, (w+1)*nd))
+      if (in_group && tg == 0) {
+        for (int g2 = 1; g2 < ng; ++g2) {
+          const float* pb = mbuf + ((g2 - 1) * wpg + wi) * mstride * 32 + lane;
+          float fa[2], fb[2];
 #pragma unroll
-      for (int mi = 0; mi < 3; ++mi) {
-        if (mi < mt) {
-          const float s0 = as.sc[mi * 16 + gq], s1 = as.sc[mi * 16 + gq + 8];
-#pragma unroll
-          for (int ni = 0; ni < 4; ++ni) {
-            if (ni < nn) {
-              acc[mi][ni][0] *= s0;
-              acc[mi][ni][1] *= s0;
-              acc[mi][ni][2] *= s1;
-              acc[mi][ni][3] *= s1;
-            }
+          for (int e = 0; e < 2; ++e) {
+            const float mo = pb[32 * e], lo = pb[64 + 32 * e];
+            const float M = fmaxf(st.m[e], mo);
+            fa[e] = st.m[e] == -INFINITY ? 0.f : exp2f(st.m[e] - M);
+            fb[e] = mo == -INFINITY ? 0.f : exp2f(mo - M);
+            st.l[e] = st.l[e] * fa[e] + lo * fb[e];
+            st.m[e] = M;
           }
 #pragma unroll
-          for (int k16 = 0; k16 < 2; ++k16) {
-            uint32_t a0, a1, a2, a3;
-            const int ar = mi * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int ac = k16 * 16 + (lane >> 4) * 8;
-            ldsm_x4(a0, a1, a2, a3, as.P + ar * 40 + ac);
+          for (int mi = 0; mi < kMaxDh / 16; ++mi)
+            if (mi < nmt)
 #pragma unroll
-            for (int ni = 0; ni < 4; ++ni) {
-              if (ni < nn) {
-                uint32_t b0, b1;
-                const int vr = k16 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int vc = warp * nd + ni * 8;
-                ldsm_x2_trans(b0, b1, as.V + vr * dpad + vc);
-                mma16816(acc[mi][ni], a0, a1, a2, a3, b0, b1);
-              }
-            }
-          }
+              for (int e = 0; e < 4; ++e)
+                st.acc[mi][e] = st.acc[mi][e] * fa[e & 1] + pb[(4 + 4 * mi + e) * 32] * fb[e & 1];
         }
       }
       math_sync();
     }
 
-    // ---- write out: directly if one split, else partial + last-block combine
-    if (nsplit == 1) {
+    // write out: directly if one split, else a partial for the combine
+    float* part = md.attn_part + static_cast<size_t>(item) * kMaxQRows * kPartStride;
+    if (in_group && tg == 0 && active) {
+      // this lane's two query columns: destination row and scale
+      float* dst[2];
+      float sc[2];
+      bool okq[2];
 #pragma unroll
-      for (int mi = 0; mi < 3; ++mi)
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni)
-          if (mi < mt && ni < nn) {
-#pragma unroll
-            for (int hrow = 0; hrow < 2; ++hrow) {
-              const int qr = mi * 16 + gq + hrow * 8;
-              if (qr < qrows) {
-                const int t = qr / grp, hh = kh * grp + qr % grp;
-                const float inv = 1.0f / as.l[qr];
-                float* o = md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh + warp * nd + ni * 8 + 2 * cq;
-                o[0] = acc[mi][ni][hrow * 2 + 0] * inv;
-                o[1] = acc[mi][ni][hrow * 2 + 1] * inv;
-              }
-            }
-          }
-    } else {
-      float* part = md.attn_part + static_cast<size_t>(item) * kMaxQRows * (kMaxDh + 2);
-#pragma unroll
-      for (int mi = 0; mi < 3; ++mi)
-#pragma unroll
-        for (int ni = 0; ni < 4; ++ni)
-          if (mi < mt && ni < nn) {
-#pragma unroll
-            for (int hrow = 0; hrow < 2; ++hrow) {
-              const int qr = mi * 16 + gq + hrow * 8;
-              if (qr < qrows) {
-                float* p = part + qr * (kMaxDh + 2) + warp * nd + ni * 8 + 2 * cq;
-                __stcg(p, acc[mi][ni][hrow * 2 + 0]);
-                __stcg(p + 1, acc[mi][ni][hrow * 2 + 1]);
-              }
-            }
-          }
-      for (int qr = tid; qr < qrows; qr += kThreads) {
-        __stcg(part + qr * (kMaxDh + 2) + kMaxDh, as.m[qr]);
-        __stcg(part + qr * (kMaxDh + 2) + kMaxDh + 1, as.l[qr]);
+      for (int e = 0; e < 2; ++e) {
+        const int qr = nt * 8 + 2 * c + e;
+        okq[e] = qr < qrows;
+        const int t = qr / grp, hh = kh * grp + qr % grp;
+        dst[e] = it.nsplit == 1 ? md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh
+                                : part + qr * kPartStride;
+        sc[e] = it.nsplit == 1 ? 1.0f / st.l[e] : 1.0f;
       }
+#pragma unroll
+      for (int mi = 0; mi < kMaxDh / 16; ++mi)
+        if (mi < nmt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (okq[e & 1]) __stcg(dst[e & 1] + attn_dim<Q8>(mt0 + mi, e < 2 ? g : g + 8), st.acc[mi][e] * sc[e & 1]);
+      if (it.nsplit > 1 && dp == 0 && g == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int qr = nt * 8 + 2 * c + e;
+          if (qr < qrows) {
+            __stcg(part + qr * kPartStride + kMaxDh, st.m[e]);
+            __stcg(part + qr * kPartStride + kMaxDh + 1, st.l[e]);
+          }
+        }
+      }
+    }
+    if (it.nsplit > 1) {
       __threadfence();
       math_sync();
       if (tid == 0) {
         const int key = si * hkv + kh;
         const uint32_t old = atomicAdd(&md.attn_tickets[key], 1u);
-        const int is_last = old + 1u == static_cast<uint32_t>(nsplit);
+        const int is_last = old + 1u == static_cast<uint32_t>(it.nsplit);
         if (is_last) md.attn_tickets[key] = 0u;
-        *as.flag = is_last;
+        *flag = is_last;
       }
       math_sync();
-      if (*as.flag) {
-        __threadfence();
-        const int item0 = sd.seq_item0[si] + kh * nsplit;
-        float* wb = wbuf + warp * kMaxSplits;
-        // one warp per query row: split weights over lanes, head dims over lanes
-        for (int qr = warp; qr < qrows; qr += kWarps) {
-          float mloc = -INFINITY;
-          for (int sp = lane; sp < nsplit; sp += 32)
-            mloc = fmaxf(mloc, __ldcg(md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + qr) * (kMaxDh + 2) + kMaxDh));
-          const float M = warp_max(mloc);
-          float lloc = 0.f;
-          for (int sp = lane; sp < nsplit; sp += 32) {
-            const float* pp = md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + qr) * (kMaxDh + 2);
-            const float ms = __ldcg(pp + kMaxDh);
-            const float w = ms == -INFINITY ? 0.f : expf(ms - M);
-            wb[sp] = w;
-            lloc = fmaf(__ldcg(pp + kMaxDh + 1), w, lloc);
-          }
-          const float inv = 1.0f / warp_sum(lloc);
-          __syncwarp();
-          float val[kMaxDh / 32];
-#pragma unroll
-          for (int e = 0; e < kMaxDh / 32; ++e) val[e] = 0.f;
-#pragma unroll 4
-          for (int sp = 0; sp < nsplit; ++sp) {
-            const float w = wb[sp];
-            const float* pp = md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + qr) * (kMaxDh + 2);
-#pragma unroll
-            for (int e = 0; e < kMaxDh / 32; ++e)
-              if (lane + 32 * e < dh) val[e] = fmaf(__ldcg(pp + lane + 32 * e), w, val[e]);
-          }
-          const int t = qr / grp, hh = kh * grp + qr % grp;
-          float* o = md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh;
-#pragma unroll
-          for (int e = 0; e < kMaxDh / 32; ++e)
-            if (lane + 32 * e < dh) o[lane + 32 * e] = val[e] * inv;
-          __syncwarp();
-        }
-      }
+      if (*flag) attn_combine(md, sd, si, kh, it.nsplit, qrows, row0, mbuf);
     }
     math_sync();
   }
+  return ok;
 }
 
-static_assert(kMaxQRows * (kMaxDh + 8) * 2 + 2 * 32 * (kMaxDh + 8) * 2 + kMaxQRows * 33 * 4 + kMaxQRows * 40 * 2 +
-                      3 * kMaxQRows * 4 + 16 + kWarps * kMaxSplits * 4 <=
-                  kPhaseBytes,
-              "attention shared memory");
 static_assert(kWarps * (2 * kMaxT * 128 + kMaxT * 10) * 4 <= kPhaseBytes, "Gated DeltaNet shared memory");
 
 // ------------------------------------------------------------------ verify
@@ -1479,13 +1702,108 @@ __device__ void verify_phase(const ModelDesc& md, const StepDesc& sd, const Smem
   }
 }
 
+// ------------------------------------------------------------ the producer
+// Lanes 0..kWarps-1 each walk one math warp's unit sequence; the warp stays
+// converged: every sweep, each lane issues its next unit if that unit's slot
+// has been released, then the sweep repeats until every lane is done. Before
+// the o_proj units of an attention layer the whole warp stops: once every
+// ring is drained it streams that layer's KV pages through the same shared
+// memory (attn_stream), then resumes the weights.
+__device__ void producer_warp(const ModelDesc& md, const StepDesc& sd, const Smem& sm, const CUtensorMap* tmk,
+                              const CUtensorMap* tmv) {
+  const int lane = threadIdx.x & 31;
+  const int w = lane < kWarps ? lane : 0;
+  const uint64_t pol = evict_first_policy();
+  int gp = -1;
+  uint32_t left = 0, tile = 0, sbl = 0, p = 0, kv_issued = 0;
+  int nsb_s = 1, sb0 = 0, nsb = 1;
+  const uint8_t* wsrc = nullptr;
+  bool done = lane >= kWarps;
+  int hold = -1;            // attention layer this lane stopped at
+  int attn_done_upto = -1;  // last attention layer whose pages were streamed
+  bool failed = false;
+  volatile int32_t* err = md.err;
+  uint64_t t_idle = 0;
+  for (uint32_t sweep = 0;; ++sweep) {
+    // advance to the next phase with units for this lane's warp
+    while (!done && left == 0 && hold < 0) {
+      const int ngp = gp + 1;
+      if (ngp > 4 * md.n_layers) { done = true; break; }
+      const int l = ngp >> 2;
+      if ((ngp & 3) == 1 && l < md.n_layers && md.layer[l].kind == MK_LAYER_FA && l > attn_done_upto) {
+        hold = l;
+        break;
+      }
+      gp = ngp;
+      const GemmDesc& g = gemm_desc(md, gp);
+      const Assign a = assign_for(g, sd.R, gridDim.x, blockIdx.x, w);
+      left = a.u1 - a.u0;
+      nsb_s = a.nsb_s;
+      tile = a.u0 / nsb_s;
+      sbl = a.u0 - tile * nsb_s;
+      sb0 = a.sb0;
+      nsb = g.nsb;
+      wsrc = g.w;
+    }
+    if (__all_sync(0xffffffffu, done || hold >= 0)) {
+      const int hl = __shfl_sync(0xffffffffu, hold, 0);
+      if (hl < 0) break;  // every lane is done
+      // every weight unit issued so far must be consumed before pages land in the ring
+      bool ok = true;
+      if (lane < kWarps && p > 0)
+        ok = mbar_wait_bounded(sm.empty(w, (p - 1) % kRing), ((p - 1) / kRing) & 1u, md, sd.barrier_timeout_ns,
+                               DEV_COPY_TIMEOUT);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) ok = attn_stream(md, sd, sm, hl, tmk, tmv, kv_issued, pol);
+      if (!ok) { failed = true; break; }
+      attn_done_upto = hl;
+      if (lane < kWarps) hold = -1;
+      continue;
+    }
+    bool issued = false;
+    if (!done && left > 0) {
+      const int slot = p % kRing;
+      if (mbar_test(sm.empty(w, slot), ((p / kRing) & 1u) ^ 1u)) {
+        uint64_t* b = sm.bar(w, slot);
+        mbar_arrive_expect_tx(b, kUnitBytes);
+        bulk_g2s(sm.ring(w, slot), wsrc + (static_cast<size_t>(tile) * nsb + sb0 + sbl) * kUnitBytes, kUnitBytes,
+                 b, pol);
+        if (++sbl == static_cast<uint32_t>(nsb_s)) { sbl = 0; ++tile; }
+        --left;
+        ++p;
+        issued = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, issued)) {
+      t_idle = 0;
+    } else if ((sweep & 63u) == 63u) {
+      // nothing could be issued: the math warps are behind; give up only on
+      // an error or after the deadline
+      if (*err != 0) break;
+      const uint64_t now = globaltimer();
+      if (t_idle == 0) t_idle = now;
+      else if (now - t_idle > sd.barrier_timeout_ns) { atomicCAS(md.err, 0, DEV_COPY_TIMEOUT); break; }
+    }
+  }
+  // the block must not exit while a copy into its shared memory is in flight
+  if (lane < kWarps)
+    for (uint32_t q = p > static_cast<uint32_t>(kRing) ? p - kRing : 0; q < p; ++q)
+      mbar_wait_bounded(sm.bar(w, q % kRing), (q / kRing) & 1u, md, 50000000ull, DEV_COPY_TIMEOUT);
+  if (failed && lane < sd.attn_ng && sd.attn_spg > 0) {
+    const AttnBuf ab = attn_buf(sm);
+    const uint32_t spg = static_cast<uint32_t>(sd.attn_spg);
+    for (uint32_t q = kv_issued > spg ? kv_issued - spg : 0; q < kv_issued; ++q)
+      mbar_wait_bounded(ab.full + lane * spg + q % spg, (q / spg) & 1u, md, 50000000ull, DEV_COPY_TIMEOUT);
+  }
+}
+
 // ------------------------------------------------------------- the kernel
 // 9 warps: at most 168 registers each (three warps share a sub-partition).
 __global__ void __launch_bounds__(kLaunchThreads, 1)
-    mk_persistent(const ModelDesc* __restrict__ mdp, const StepDesc* __restrict__ sdp, float* attn_scratch) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+    mk_persistent(const ModelDesc* __restrict__ mdp, const StepDesc* __restrict__ sdp, float* attn_scratch,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   __shared__ int sflag;
-  const Smem sm{smem_raw};
+  const Smem sm{};
   const ModelDesc& md = *mdp;
   const StepDesc& sd = *sdp;
   const int warp = threadIdx.x >> 5;
@@ -1493,10 +1811,15 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
     mbar_init(sm.bar(threadIdx.x / kRing, threadIdx.x % kRing), 1);
     mbar_init(sm.empty(threadIdx.x / kRing, threadIdx.x % kRing), 1);
   }
+  if (threadIdx.x < kAttnMaxSlots) {
+    const AttnBuf ab = attn_buf(sm);
+    mbar_init(ab.full + threadIdx.x, 1);
+    mbar_init(ab.empty + threadIdx.x, sd.attn_wpg > 0 ? sd.attn_wpg : 1);
+  }
   mbar_fence_init();
   __syncthreads();
   if (warp == kWarps) {  // the producer warp
-    producer_warp(md, sd, sm);
+    producer_warp(md, sd, sm, &tm_k, &tm_v);
     return;
   }
   WarpCtx wc;
@@ -1504,6 +1827,7 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
   wc.lane = threadIdx.x & 31;
   wc.gid = blockIdx.x * kWarps + wc.warp;
   wc.c_pos = 0;
+  wc.kv_pos = 0;
 
   int nbar = 0;
   float* my_scratch = attn_scratch + static_cast<size_t>(blockIdx.x) * kWarps * 2 * kMaxDh;
@@ -1525,7 +1849,9 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
       const int l = (ph - 1) / 5, part = (ph - 1) % 5;
       if (part == 1) {
         if (md.layer[l].kind == MK_LAYER_GDN) gdn_phase(md, sd, l, wc, sm);
-        else attn_phase(md, sd, l, sm, my_scratch);
+        else if (!md.kv_q8) ok = attn_phase<false, true>(md, sd, l, sm, my_scratch, wc);
+        else if (md.dh % 128 == 0) ok = attn_phase<true, true>(md, sd, l, sm, my_scratch, wc);
+        else ok = attn_phase<true, false>(md, sd, l, sm, my_scratch, wc);
       } else {
         gp = 4 * l + (part == 0 ? 0 : part - 1);
       }
@@ -1539,8 +1865,9 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
 }
 
 cudaError_t launch_persistent(const ModelDesc* md, const StepDesc* sd, float* attn_scratch, int grid,
-                              cudaStream_t stream) {
-  void* args[] = {const_cast<ModelDesc**>(&md), const_cast<StepDesc**>(&sd), &attn_scratch};
+                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, cudaStream_t stream) {
+  void* args[] = {const_cast<ModelDesc**>(&md), const_cast<StepDesc**>(&sd), &attn_scratch,
+                  const_cast<CUtensorMap*>(tm_k), const_cast<CUtensorMap*>(tm_v)};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(mk_persistent), dim3(grid), dim3(kLaunchThreads),
                                      args, kSmemBytes, stream);
 }

@@ -7,8 +7,8 @@ Tolerances (the verify step's stated parity bar):
   tokens, counts, page tables: exact, except rows whose oracle top-2 logit gap
                  is below 1e-3 * rms(logits) (and every later row of that
                  sequence), which are counted and reported
-  KV codes       new positions: q8 codes within 1 (exact on identical fp32
-                 inputs), fp16 within one binary16 step plus 1e-4 * rms; counted
+  KV entries     new positions: q8 codes within 1 (exact on identical fp32
+                 inputs); fp16 head vectors within relative L2 1e-3; counted
 """
 from __future__ import annotations
 
@@ -112,11 +112,11 @@ class Pair:
     def compare_kv(self, seq, positions):
         """New positions of one sequence in every attention layer.
 
-        fp16 pool: decoded values within one binary16 step of the element
-        (2^-10 |x|) plus 1e-4 * rms of the stored head vector (the inputs differ
-        by fp32-vs-fp64 rounding, so an element on a rounding boundary lands one
-        step away and near-zero elements a few steps). q8 pool: codes within 1
-        and scales within one binary16 step. Returns the number of differing
+        fp16 pool: every stored head vector within relative L2 1e-3 of the
+        oracle's (the state bar: the entries are projections of the hidden
+        state, whose upstream error grows with depth, plus one binary16
+        rounding of 2^-11 relative at most). q8 pool: codes within 1 and
+        scales within one binary16 step. Returns the number of differing
         elements."""
         views = self.eng.kv_views()
         table = self.oracle.seq_get(seq)["pages"]
@@ -130,10 +130,8 @@ class Pair:
                 if name in ("k", "v"):
                     gf = gg.view(np.float16).astype(np.float64)
                     of = oo.view(np.float16).astype(np.float64)
-                    rms = np.sqrt(np.mean(of ** 2, axis=-1, keepdims=True))
-                    err = np.abs(gf - of)
-                    bound = 2.0 ** -10 * np.abs(of) + 1e-4 * rms + 1e-30
-                    assert np.all(err <= bound), f"{name}: max err/bound {np.max(err / bound)}"
+                    rel = np.linalg.norm(gf - of, axis=-1) / np.maximum(np.linalg.norm(of, axis=-1), 1e-30)
+                    assert np.all(rel <= REL_L2_TOL), f"{name}: max rel L2 {np.max(rel)}"
                     d = gg != oo
                 else:
                     d = np.abs(gg.astype(np.int32) - oo.astype(np.int32))
