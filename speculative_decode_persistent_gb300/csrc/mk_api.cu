@@ -432,7 +432,7 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
     gemm(ld.in, p.in[l], PRO_RMS_X, EPI_STORE_YIN, reinterpret_cast<const float*>(packed + p.off_attn_norm[l]));
     gemm(ld.o, p.o[l], gdn ? PRO_GDN_OUT : PRO_FA_OUT, EPI_RESID_X,
          gdn ? reinterpret_cast<const float*>(packed + p.off_onorm[l]) : nullptr);
-    gemm(ld.gu, p.gu[l], PRO_RMS_X, EPI_SWIGLU_H, reinterpret_cast<const float*>(packed + p.off_ffn_norm[l]));
+    gemm(ld.gu, p.gu[l], PRO_RMS_X, EPI_STORE_GU, reinterpret_cast<const float*>(packed + p.off_ffn_norm[l]));
     gemm(ld.down, p.down[l], PRO_H, EPI_RESID_X, nullptr);
     ld.conv_w = gdn ? reinterpret_cast<const float*>(packed + p.off_conv[l]) : nullptr;
   }

@@ -67,7 +67,11 @@ constexpr int kAttnBarOff = 3840;             // byte offset of those mbarriers 
 // ------------------------------------------------------------- descriptors
 enum Prologue : int32_t { PRO_RMS_X = 0, PRO_GDN_OUT = 1, PRO_FA_OUT = 2, PRO_H = 3 };
 enum ZeroBuf : int32_t { ZERO_NONE = 0, ZERO_GU = 1, ZERO_YIN = 2 };
-enum Epilogue : int32_t { EPI_STORE_YIN = 0, EPI_RESID_X = 1, EPI_SWIGLU_H = 2, EPI_TOP2 = 3 };
+// Outputs of one GEMM phase: input projections into yin, residual add into x
+// (then the 32-wide sums of squares for the next RMSNorm), gate/up pairs into
+// gu (the SwiGLU is applied by the down projection's prologue), logits into
+// the per-warp top-1 records.
+enum Epilogue : int32_t { EPI_STORE_YIN = 0, EPI_RESID_X = 1, EPI_STORE_GU = 2, EPI_TOP2 = 3 };
 
 struct GemmDesc {
   const uint8_t* w;  // units [n_tiles][nsb]
@@ -118,8 +122,8 @@ struct ModelDesc {
   float* xsq;        // [H/32][kMaxRows] sums of squares of x over each 32-wide chunk
   float* yin;        // [kMaxRows][n_in_max] input projections
   float* o;          // [kMaxRows][o_stride] mixer outputs
-  float* h;          // [kMaxRows][F] SwiGLU output
-  float* gu;         // [kMaxRows][2F] gate/up outputs of split tiles (summed by red.add)
+  float* h;          // [kMaxRows][F] SwiGLU output (written only while debug outputs are on)
+  float* gu;         // [kMaxRows][2F] gate/up outputs, 16-row blocks of 8 gate + 8 up rows
   float* logits;     // [kMaxRows][V] lm_head outputs of split tiles (summed by red.add)s
   float* partial;    // [grid*kWarps][max_seg][kMaxRows][32]
   uint32_t* tickets; // per tile

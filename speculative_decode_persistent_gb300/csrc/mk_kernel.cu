@@ -400,8 +400,10 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
         } else if (g.pro == PRO_FA_OUT) {
           s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
           s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.hq * md.dh + k));
-        } else {
-          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.h + static_cast<size_t>(r) * md.F + k));
+        } else {  // SwiGLU of the gate/up pair: 4 consecutive f share one 8-row block
+          const float* gr = md.gu + static_cast<size_t>(r) * 2 * md.F + (k >> 3) * 16 + (k & 7);
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(gr));
+          s2[b] = __ldcg(reinterpret_cast<const float4*>(gr + 8));
         }
       }
     }
@@ -448,7 +450,10 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
           u[0] = s1[b].x * sigmoidf_(s2[b].x); u[1] = s1[b].y * sigmoidf_(s2[b].y);
           u[2] = s1[b].z * sigmoidf_(s2[b].z); u[3] = s1[b].w * sigmoidf_(s2[b].w);
         } else {
-          u[0] = s1[b].x; u[1] = s1[b].y; u[2] = s1[b].z; u[3] = s1[b].w;
+          u[0] = siluf_(s1[b].x) * s2[b].x; u[1] = siluf_(s1[b].y) * s2[b].y;
+          u[2] = siluf_(s1[b].z) * s2[b].z; u[3] = siluf_(s1[b].w) * s2[b].w;
+          if (md.dbg_logits)  // debug outputs on: keep the SwiGLU rows for mk_debug_scratch
+            *reinterpret_cast<float4*>(md.h + static_cast<size_t>(r) * md.F + k) = make_float4(u[0], u[1], u[2], u[3]);
         }
         put_act(act, cs2, R, sx, r, kl, u, lane);
       }
@@ -510,16 +515,13 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
         }
       break;
     }
-    case EPI_SWIGLU_H: {
-      const int pos = lane & 15;
-      const int f = (static_cast<int>(tile) * 2 + (lane >> 4)) * 8 + (pos & 7);
+    case EPI_STORE_GU:
+      if (!summed && n < g.n_out) {
 #pragma unroll
-      for (int r = 0; r < 4 * NT; ++r) {
-        const float up = __shfl_down_sync(0xffffffffu, v[r], 8);
-        if (r < R && pos < 8 && f < md.F) md.h[static_cast<size_t>(r) * md.F + f] = siluf_(v[r]) * up;
+        for (int r = 0; r < 4 * NT; ++r)
+          if (r < R) md.gu[static_cast<size_t>(r) * 2 * md.F + n] = v[r];
       }
       break;
-    }
     case EPI_TOP2:
       if (TOP) {
         float* rec = top_rec(warp);
@@ -637,9 +639,12 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) bcol[nt] = act + min(nt * 8 + gq, 2 * R - 1) * cstride + cq * 16;
   // where split tiles are summed
-  float* dst = g.epi == EPI_STORE_YIN ? md.yin : g.epi == EPI_RESID_X ? md.x : g.epi == EPI_SWIGLU_H ? md.gu : md.logits;
+  float* dst = g.epi == EPI_STORE_YIN ? md.yin : g.epi == EPI_RESID_X ? md.x : g.epi == EPI_STORE_GU ? md.gu : md.logits;
   const int dstride = g.epi == EPI_STORE_YIN ? md.n_in_max : g.epi == EPI_RESID_X ? md.H
-                      : g.epi == EPI_SWIGLU_H ? 2 * md.F : md.V;
+                      : g.epi == EPI_STORE_GU ? 2 * md.F : md.V;
+  // stores and split logits need no completion step: the summed buffer is the
+  // output (split logits are scanned by lm_argmax after the next barrier)
+  const bool no_ticket = g.epi == EPI_STORE_YIN || g.epi == EPI_STORE_GU || (TOP && a.sc.S > 1);
   if (TOP) {
     float* rec = top_rec(wc.warp);
     if (lane < R) {
@@ -687,7 +692,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
       for (int r = 0; r < 4 * NT; ++r)
         if (r < R) atomicAdd(dst + static_cast<size_t>(r) * dstride + n, v[r]);
     }
-    if (g.epi == EPI_STORE_YIN) return;  // the sum itself is the output
+    if (no_ticket) return;
     __threadfence();
     __syncwarp();
     uint32_t last = 0;
@@ -1659,6 +1664,56 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
 
 static_assert(kWarps * (2 * kMaxT * 128 + kMaxT * 10) * 4 <= kPhaseBytes, "Gated DeltaNet shared memory");
 
+// ------------------------------------------------------------ lm argmax
+// When lm_head's reduction is sliced, every tile is split and its logits were
+// summed in md.logits; after the barrier each warp scans tiles gid, gid +
+// (warps), ... and merges them into its top-1 record (ties: lowest index).
+__device__ __noinline__ void lm_argmax(const ModelDesc& md, const StepDesc& sd, const WarpCtx& wc) {
+  const int R = sd.R, lane = wc.lane;
+  const int nw = gridDim.x * kWarps;
+  const int ntile = (md.V + kTileRows - 1) / kTileRows;
+  float b[kMaxRows];
+  int bi[kMaxRows];
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) {
+    b[r] = -FLT_MAX;
+    bi[r] = 0x7fffffff;
+  }
+  for (int t = wc.gid; t < ntile; t += nw) {
+    const int n = t * kTileRows + lane;
+    if (n < md.V) {
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r)
+        if (r < R) {
+          const float x = __ldcg(md.logits + static_cast<size_t>(r) * md.V + n);
+          if (!isfinite(x)) atomicOr(&md.err[1], 1);
+          if (md.dbg_logits) md.dbg_logits[static_cast<size_t>(r) * md.V + n] = x;
+          top1_merge(b[r], bi[r], x, n);
+        }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r)
+    if (r < R) {
+      float x = b[r];
+      int ix = bi[r];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ox = __shfl_xor_sync(0xffffffffu, x, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
+        top1_merge(x, ix, ox, oi);
+      }
+      if (lane == 0) {
+        const size_t at = static_cast<size_t>(wc.gid) * kMaxRows + r;
+        float rb = md.top_val[at];
+        int ri = md.top_idx[at];
+        top1_merge(rb, ri, x, ix);
+        md.top_val[at] = rb;
+        md.top_idx[at] = ri;
+      }
+    }
+}
+
 // ------------------------------------------------------------------ verify
 // Block 0: argmax of every row over all warps' top-2 records (lowest index on
 // exact ties), then per sequence the longest prefix of drafts that equal the
@@ -1858,9 +1913,14 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
     }
     if (gp >= 0) ok = gemm_dispatch(md, sd, gp, sm, wc);
     // a failed wait inside a phase still meets the barrier, which reports it
-    const bool synced = grid_sync(md, sd, nbar, &sflag);
+    bool synced = grid_sync(md, sd, nbar, &sflag);
     if (md.dbg_time && blockIdx.x == 0 && threadIdx.x == 0) md.dbg_time[ph + 1] = globaltimer();
     if (!synced || !ok) break;
+    if (ph == n_phases - 2 && make_sched(md.lm.nsb, sd.R).S > 1) {  // sliced lm_head: scan the summed logits
+      lm_argmax(md, sd, wc);
+      synced = grid_sync(md, sd, nbar, &sflag);
+      if (!synced) break;
+    }
   }
 }
 
