@@ -93,7 +93,8 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint3
 }
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  // registers only: not volatile, so the scheduler may interleave independent chains
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -384,19 +385,22 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
   const int total = R * per_row;
   const int nchunk = md.H / 32;
   for (int base = 0; base < total; base += kThreads * kB) {
-    float4 s1[kB], s2[kB];
+    // every source of this round, norm gains included, is loaded before any is used
+    float4 s1[kB], s2[kB], s3[kB];
     float sq[kMaxRows];
 #pragma unroll
     for (int b = 0; b < kB; ++b) {
       const int idx = base + b * kThreads + tid;
-      s1[b] = s2[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+      s1[b] = s2[b] = s3[b] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (idx < total) {
         const int r = idx / per_row, k = k0 + (idx - r * per_row) * 4;
         if (g.pro == PRO_RMS_X) {
           s1[b] = __ldcg(reinterpret_cast<const float4*>(md.x + static_cast<size_t>(r) * md.H + k));
+          s2[b] = *reinterpret_cast<const float4*>(g.gain + k);
         } else if (g.pro == PRO_GDN_OUT) {
           s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
           s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.conv_ch + k));
+          s3[b] = *reinterpret_cast<const float4*>(g.gain + k % md.dv);
         } else if (g.pro == PRO_FA_OUT) {
           s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
           s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.hq * md.dh + k));
@@ -435,15 +439,14 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
         const int r = idx / per_row, kl = (idx - r * per_row) * 4, k = k0 + kl;
         float u[4];
         if (g.pro == PRO_RMS_X) {
-          const float4 gg = *reinterpret_cast<const float4*>(g.gain + k);
+          const float4 gg = s2[b];
           const float sc = misc[r];
           u[0] = s1[b].x * sc * gg.x; u[1] = s1[b].y * sc * gg.y; u[2] = s1[b].z * sc * gg.z; u[3] = s1[b].w * sc * gg.w;
         } else if (g.pro == PRO_GDN_OUT) {
           float hs = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, s1[b].w * s1[b].w)));
           for (int off = 1; off < md.dv / 4; off <<= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
           const float sc = 1.0f / sqrtf(hs / static_cast<float>(md.dv) + md.eps);
-          const int i = k % md.dv;
-          const float4 gg = *reinterpret_cast<const float4*>(g.gain + i);
+          const float4 gg = s3[b];
           u[0] = s1[b].x * sc * gg.x * siluf_(s2[b].x); u[1] = s1[b].y * sc * gg.y * siluf_(s2[b].y);
           u[2] = s1[b].z * sc * gg.z * siluf_(s2[b].z); u[3] = s1[b].w * sc * gg.w * siluf_(s2[b].w);
         } else if (g.pro == PRO_FA_OUT) {
