@@ -41,6 +41,30 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def measured_traffic(algorithmic):
+    """DRAM bytes per launch from the committed ncu capture (profiles/
+    mk_persistent_traffic.json), scaled to this workload by the measured
+    traffic/algorithmic ratio; None when the kernel sources changed since the
+    capture (the counters would no longer describe this kernel)."""
+    import glob
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "mk_persistent_traffic.json")) as f:
+            rec = json.load(f)
+        srcs = sorted(glob.glob(os.path.join(ROOT, "speculative_decode_persistent_gb300", "csrc", "*.cu")) +
+                      glob.glob(os.path.join(ROOT, "speculative_decode_persistent_gb300", "csrc", "*.cuh")) +
+                      [os.path.join(ROOT, "include", "mk.h")])
+        h = hashlib.sha256()
+        for fn in srcs:
+            with open(fn, "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["kernel_sources_sha256"]:
+            return None
+        return algorithmic * rec["traffic_over_algorithmic"]
+    except Exception:
+        return None
+
+
 def algorithmic_bytes(model, kv_q8, seqs):
     """Bytes the step must move: every streamed weight once, the embedding rows
     it gathers, each sequence's cached K/V once per attention layer plus the
@@ -178,6 +202,18 @@ def run_reference(args, world, rank):
     print(json.dumps(line))
 
 
+def layer_override(args):
+    """--layers N: the same widths with only the first N layers (profiling
+    stand-in that fits an ncu capture; never a headline number)."""
+    if not args.layers:
+        return None
+    from gen.configs import WORKLOADS
+    m = dict(WORKLOADS[args.workload]["model"])
+    m["kinds"] = list(m["kinds"])[: args.layers]
+    m["n_layers"] = args.layers
+    return dict(model=m)
+
+
 def len_rows(workload):
     from gen.configs import WORKLOADS
     return sum(T for _c, T in WORKLOADS[workload]["seqs"])
@@ -191,7 +227,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     t_setup = time.perf_counter()
-    wl = Workload(args.workload, nthreads=os.cpu_count())
+    wl = Workload(args.workload, nthreads=os.cpu_count(), overrides=layer_override(args))
     eng = mk.Engine(wl.model, wl.weights, wl.kv_q8, wl.n_pages, max_seqs=wl.max_seqs, device=f"cuda:{local}")
     eng.load_pool(wl.pool)
     for s, (cached, _T) in enumerate(wl.seqs):
@@ -260,13 +296,14 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "q4-weights/f16-split-mma/f32",
             "data": "synthetic (seeded random-init weights and caches)",
-            "config": {"workload": args.workload, "rows_per_step": R, "sequences": len(wl.seqs),
+            "config": {"workload": args.workload if not args.layers else f"{args.workload} (first {args.layers} layers: profiling stand-in)",
+                       "rows_per_step": R, "sequences": len(wl.seqs),
                        "cached_tokens": [c for c, _T in wl.seqs], "kv": "q8" if wl.kv_q8 else "fp16",
                        "l2": "inputs larger than L2: 14.4 GB of weights streamed per step",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "step_us": ms * 1e3,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": measured_traffic(ab["total"]),
                          "algorithmic_bytes": ab["total"], "bytes_breakdown": ab,
                          "kernel": "mk_persistent (whole step, one cooperative launch)",
                          "frac_of_8TBs": achieved / 8000.0},
@@ -314,6 +351,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="profiling stand-in: keep only the first N layers")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)
