@@ -290,6 +290,23 @@ mk_status mk_step_static(mk_ctx* ctx, int32_t n_rows, const int32_t* tokens, con
                          const int32_t* seq_ids, const uint8_t* row_flags, int32_t* out_tokens,
                          int32_t* out_counts);
 
+/*
+ * Test hook, host only (no context, no device work): the split of one GEMM
+ * phase of n_tiles tiles x nsb super-blocks at `rows` rows over `grid`
+ * blocks, exactly as the kernel computes it. warp_info (host, grid x
+ * warps-per-block x 4 int32, block-major) receives per math warp: the first
+ * super-block of its slice of the reduction, the slice width, and its unit
+ * range [u0, u1) inside the slice (units are tile-major, super-block-minor).
+ * tile_arrivals (host, n_tiles int32) receives, per tile, how many partial
+ * contributions its completion ticket waits for. Returns the number of math
+ * warps per block, or MK_ERR_INVALID.
+ */
+int32_t mk_debug_gemm_schedule(int32_t n_tiles, int32_t nsb, int32_t rows, int32_t grid,
+                               int32_t* warp_info, int32_t* tile_arrivals);
+/* Test hook, host only: shared-memory bytes of the activation operand for a
+ * slice of nsb_slice super-blocks at `rows` rows (must fit the kernel's
+ * activation region). */
+int32_t mk_debug_act_bytes(int32_t nsb_slice, int32_t rows);
 const char* mk_status_str(mk_status status);
 
 #ifdef __cplusplus

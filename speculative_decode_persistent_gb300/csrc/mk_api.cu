@@ -969,3 +969,24 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
   }
   return h[kOutInts + 1] ? MK_ERR_NONFINITE : MK_OK;
 }
+
+extern "C" int32_t mk_debug_gemm_schedule(int32_t n_tiles, int32_t nsb, int32_t rows, int32_t grid,
+                                          int32_t* warp_info, int32_t* tile_arrivals_out) {
+  if (n_tiles < 1 || nsb < 1 || rows < 1 || rows > kMaxRows || grid < 1 || !warp_info || !tile_arrivals_out)
+    return MK_ERR_INVALID;
+  for (int cta = 0; cta < grid; ++cta)
+    for (int w = 0; w < kWarps; ++w) {
+      const Assign a = assign_units(n_tiles, nsb, rows, grid, cta, w);
+      int32_t* o = warp_info + (static_cast<size_t>(cta) * kWarps + w) * 4;
+      o[0] = a.sb0;
+      o[1] = a.nsb_s;
+      o[2] = static_cast<int32_t>(a.u0);
+      o[3] = static_cast<int32_t>(a.u1);
+    }
+  const Sched sc = make_sched(nsb, rows);
+  for (int t = 0; t < n_tiles; ++t)
+    tile_arrivals_out[t] = static_cast<int32_t>(tile_arrivals(sc, n_tiles, nsb, grid, static_cast<uint32_t>(t)));
+  return kWarps;
+}
+
+extern "C" int32_t mk_debug_act_bytes(int32_t nsb_slice, int32_t rows) { return act_bytes(nsb_slice, rows); }

@@ -278,4 +278,42 @@ __host__ __device__ inline uint32_t segments_in(uint32_t Us, uint32_t Ws, uint32
   return warp_of_unit(Us, Ws, b - 1) - warp_of_unit(Us, Ws, a) + 1;
 }
 
+// One math warp's share of a GEMM phase of n_tiles x nsb units at R rows on
+// `grid` blocks: its slice of the reduction, and units [u0, u1) of that
+// slice (tile-major, super-block-minor).
+struct Assign {
+  Sched sc;
+  int sl, nsb_s, sb0, cta0;
+  uint32_t Us, Ws, ws, u0, u1;
+};
+
+__host__ __device__ inline Assign assign_units(int n_tiles, int nsb, int R, int grid, int cta, int warp) {
+  Assign a;
+  a.sc = make_sched(nsb, R);
+  a.sl = slice_of_cta(a.sc, grid, cta);
+  a.cta0 = slice_cta0(a.sc, grid, a.sl);
+  const int cta1 = slice_cta0(a.sc, grid, a.sl + 1);
+  a.nsb_s = slice_nsb(a.sc, nsb, a.sl);
+  a.sb0 = slice_sb0(a.sc, a.sl);
+  a.Us = static_cast<uint32_t>(n_tiles) * a.nsb_s;
+  a.Ws = static_cast<uint32_t>(cta1 - a.cta0) * kWarps;
+  a.ws = static_cast<uint32_t>(cta - a.cta0) * kWarps + warp;
+  a.u0 = warp_u0(a.Us, a.Ws, a.ws);
+  a.u1 = warp_u0(a.Us, a.Ws, a.ws + 1);
+  return a;
+}
+
+// Contributions a split tile's completion ticket waits for: one per warp
+// range holding any of its units, over every slice.
+__host__ __device__ inline uint32_t tile_arrivals(const Sched& sc, int n_tiles, int nsb, int grid, uint32_t tile) {
+  uint32_t na = 0;
+  for (int sl = 0; sl < sc.S; ++sl) {
+    const uint32_t ns = slice_nsb(sc, nsb, sl);
+    const uint32_t Us = static_cast<uint32_t>(n_tiles) * ns;
+    const uint32_t Ws = static_cast<uint32_t>(slice_cta0(sc, grid, sl + 1) - slice_cta0(sc, grid, sl)) * kWarps;
+    na += segments_in(Us, Ws, tile * ns, tile * ns + ns);
+  }
+  return na;
+}
+
 }  // namespace mk

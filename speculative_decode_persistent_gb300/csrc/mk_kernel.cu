@@ -219,26 +219,8 @@ __device__ __forceinline__ const GemmDesc& gemm_desc(const ModelDesc& md, int gp
   return part == 0 ? L.in : part == 1 ? L.o : part == 2 ? L.gu : L.down;
 }
 
-struct Assign {
-  Sched sc;
-  int sl, nsb_s, sb0, cta0;
-  uint32_t Us, Ws, ws, u0, u1;
-};
-
 __device__ __forceinline__ Assign assign_for(const GemmDesc& g, int R, int grid, int cta, int warp) {
-  Assign a;
-  a.sc = make_sched(g.nsb, R);
-  a.sl = slice_of_cta(a.sc, grid, cta);
-  a.cta0 = slice_cta0(a.sc, grid, a.sl);
-  const int cta1 = slice_cta0(a.sc, grid, a.sl + 1);
-  a.nsb_s = slice_nsb(a.sc, g.nsb, a.sl);
-  a.sb0 = slice_sb0(a.sc, a.sl);
-  a.Us = static_cast<uint32_t>(g.n_tiles) * a.nsb_s;
-  a.Ws = static_cast<uint32_t>(cta1 - a.cta0) * kWarps;
-  a.ws = static_cast<uint32_t>(cta - a.cta0) * kWarps + warp;
-  a.u0 = warp_u0(a.Us, a.Ws, a.ws);
-  a.u1 = warp_u0(a.Us, a.Ws, a.ws + 1);
-  return a;
+  return assign_units(g.n_tiles, g.nsb, R, grid, cta, warp);
 }
 
 // Bounded wait for an mbarrier phase; false (and the error word set) on timeout
@@ -700,14 +682,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
     __syncwarp();
     uint32_t last = 0;
     if (lane == 0) {
-      uint32_t na = 0;
-      for (int sl = 0; sl < a.sc.S; ++sl) {
-        const uint32_t ns = slice_nsb(a.sc, g.nsb, sl);
-        const uint32_t Us = static_cast<uint32_t>(g.n_tiles) * ns;
-        const uint32_t Ws =
-            static_cast<uint32_t>(slice_cta0(a.sc, grid, sl + 1) - slice_cta0(a.sc, grid, sl)) * kWarps;
-        na += segments_in(Us, Ws, tile * ns, tile * ns + ns);
-      }
+      const uint32_t na = tile_arrivals(a.sc, g.n_tiles, g.nsb, grid, tile);
       const uint32_t old = atomicAdd(&md.tickets[tile], 1u);
       last = (old + 1u == na) ? 1u : 0u;
       if (last) md.tickets[tile] = 0u;

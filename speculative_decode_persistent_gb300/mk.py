@@ -93,6 +93,8 @@ def _load():
         "mk_step_io_bytes": (i32, [vp, P(u64), P(u64)]),
         "mk_step_static": (i32, [vp, i32, vp, vp, vp, vp, vp, vp]),
         "mk_debug_timeline": (i32, [vp, vp]),
+        "mk_debug_gemm_schedule": (i32, [i32, i32, i32, i32, vp, vp]),
+        "mk_debug_act_bytes": (i32, [i32, i32]),
         "mk_status_str": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -109,7 +111,19 @@ EXPORTS = ["mk_packed_bytes", "mk_kv_bytes", "mk_kv_scale_bytes", "mk_gdn_state_
            "mk_step", "mk_step_prepare", "mk_step_launch", "mk_step_finish", "mk_commit",
            "mk_debug_outputs", "mk_last_launch_ms", "mk_debug_skip_arrival", "mk_grid_blocks",
            "mk_status_str", "mk_debug_scratch", "mk_step_io_bytes", "mk_step_static",
-           "mk_debug_timeline"]
+           "mk_debug_timeline", "mk_debug_gemm_schedule", "mk_debug_act_bytes"]
+
+
+def gemm_schedule(n_tiles: int, nsb: int, rows: int, grid: int):
+    """Host-only test hook: the kernel's split of one GEMM phase.
+    Returns (warp_info [grid*warps][4]: sb0, nsb_slice, u0, u1; tile_arrivals [n_tiles])."""
+    import numpy as np
+    info = np.zeros((grid * 16, 4), np.int32)  # room for up to 16 math warps per block
+    arr = np.zeros(n_tiles, np.int32)
+    nw = lib.mk_debug_gemm_schedule(n_tiles, nsb, rows, grid, info.ctypes.data, arr.ctypes.data)
+    if nw < 0:
+        raise MkError(nw, "mk_debug_gemm_schedule")
+    return info[: grid * nw].reshape(grid, nw, 4), arr
 
 
 def _np_ptr(a):
