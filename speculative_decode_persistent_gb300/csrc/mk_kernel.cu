@@ -861,14 +861,24 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
       return tau < 0 ? __ldcg(hist + (3 + tau) * C + ch)
                      : __ldcg(md.yin + static_cast<size_t>(row0 + tau) * md.n_in_max + ch);
     };
-    auto conv = [&](int ch, int t) -> float {
-      const float* w = cw + ch * 4;
-      float c = w[0] * pre(ch, t - 3);
-      c = fmaf(w[1], pre(ch, t - 2), c);
-      c = fmaf(w[2], pre(ch, t - 1), c);
-      c = fmaf(w[3], pre(ch, t), c);
-      return siluf_(c);
+    // causal conv + SiLU of channel ch at row t; when `hist_out` the channel's
+    // history after row t (inputs t-2, t-1, t) goes straight to that row's
+    // state slot from the values already loaded
+    auto conv = [&](int ch, int t, bool hist_out) -> float {
+      const float4 w = *reinterpret_cast<const float4*>(cw + ch * 4);
+      const float p0 = pre(ch, t - 3), p1 = pre(ch, t - 2), p2 = pre(ch, t - 1), p3 = pre(ch, t);
+      if (hist_out && (sd.seq_snap_all[si] || t == T - 1)) {
+        const size_t ss = static_cast<size_t>(seq) * md.n_slots + sd.seq_slot_out[si][t];
+        float* ho = md.conv_state + (ss * md.n_gdn + gi) * 3 * C + ch;
+        __stcg(ho, p1);
+        __stcg(ho + C, p2);
+        __stcg(ho + 2 * C, p3);
+      }
+      return siluf_(fmaf(w.w, p3, fmaf(w.z, p2, fmaf(w.y, p1, w.x * p0))));
     };
+    // q/k history is written once per qk head: by the tasks of its first
+    // v-head, each for its own 8 channels of q and of k
+    const bool qk_owner = h % (hv / hk) == 0;
     // normalised q, k of this head for every row: [t][dk] each, per warp
     float* qs = reinterpret_cast<float*>(sm.phase()) + wc.warp * (2 * kMaxT * 128 + kMaxT * 10);
     float* ks = qs + kMaxT * 128;
@@ -885,8 +895,9 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
           q4[e] = k4[e] = 0.f;
           if (e < ne) {
             const int d = lane + 32 * e;
-            q4[e] = conv(g * dk + d, t);
-            k4[e] = conv(hk * dk + g * dk + d, t);
+            const bool own = qk_owner && d >= i0 && d < i0 + 8;
+            q4[e] = conv(g * dk + d, t, own);
+            k4[e] = conv(hk * dk + g * dk + d, t, own);
             sq = fmaf(q4[e], q4[e], sq);
             sk = fmaf(k4[e], k4[e], sk);
           }
@@ -900,7 +911,7 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
             qs[t * 128 + lane + 32 * e] = q4[e] * iq;
             ks[t * 128 + lane + 32 * e] = k4[e] * ik;
           }
-        if (lane < 8) vs[t * 8 + lane] = conv(2 * hk * dk + h * dv + i0 + lane, t);
+        if (lane < 8) vs[t * 8 + lane] = conv(2 * hk * dk + h * dv + i0 + lane, t, true);
         if (lane == 0) {
           const float* yr = md.yin + static_cast<size_t>(row0 + t) * md.n_in_max;
           gs[t * 2 + 0] = sigmoidf_(__ldcg(yr + a_off + h));
@@ -969,23 +980,6 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
 #pragma unroll
         for (int ii = 1; ii < 8; ++ii) ov = lane == ii ? sov[ii] : ov;
         md.o[static_cast<size_t>(row0 + t) * md.o_stride + h * dv + i0 + lane] = ov;
-      }
-    }
-    // convolution history after each row, for the channels this task owns
-    if (lane < 8) {
-      int chs[3];
-      int nch = 0;
-      chs[nch++] = 2 * hk * dk + h * dv + i0 + lane;
-      if (h % (hv / hk) == 0) {
-        chs[nch++] = g * dk + i0 + lane;
-        chs[nch++] = hk * dk + g * dk + i0 + lane;
-      }
-      for (int t = 0; t < T; ++t) {
-        if (!(sd.seq_snap_all[si] || t == T - 1)) continue;
-        const size_t ss = static_cast<size_t>(seq) * md.n_slots + sd.seq_slot_out[si][t];
-        float* ho = md.conv_state + (ss * md.n_gdn + gi) * 3 * C;
-        for (int c = 0; c < nch; ++c)
-          for (int j = 0; j < 3; ++j) __stcg(ho + j * C + chs[c], pre(chs[c], t - 2 + j));
       }
     }
     __syncwarp();
