@@ -133,8 +133,8 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
-__device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + expf(-v)); }
-__device__ __forceinline__ float siluf_(float v) { return v / (1.0f + expf(-v)); }
+__device__ __forceinline__ float sigmoidf_(float v) { return __fdividef(1.0f, 1.0f + __expf(-v)); }
+__device__ __forceinline__ float siluf_(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // --------------------------------------------------------- shared memory
 // The block's dynamic shared memory. Every region is addressed from this
