@@ -55,6 +55,8 @@ WORKLOADS = {
                  cache_seed=1, draft_seed=2),
     "qwen27-t1-4k-fp16": dict(model=QWEN27, kv_q8=0, n_pages=320, seqs=[(4096, 1)],
                               weight_seed=0, cache_seed=1, draft_seed=2),
+    "qwen27-t5-4k-fp16": dict(model=QWEN27, kv_q8=0, n_pages=320, seqs=[(4096, 5)],
+                              weight_seed=0, cache_seed=1, draft_seed=2),
     "qwen27-t5-4k-fp16-mtp": dict(model=dict(QWEN27, has_mtp=1, draft_vocab=32768),
                                   kv_q8=0, n_pages=320, seqs=[(4096, 5)], n_draft=4,
                                   weight_seed=0, cache_seed=1, draft_seed=2),

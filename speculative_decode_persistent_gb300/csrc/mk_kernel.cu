@@ -322,22 +322,22 @@ __device__ __forceinline__ int act_perm(int kl) {
 
 __device__ __forceinline__ void put_act(__half* act, int cs2, int R, float* sx, int r, int kl, const float (&u)[4],
                                         int lane) {
-  __half hi[4], lo[4];
-  float part = 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    hi[e] = __float2half_rn(u[e]);
-    lo[e] = __float2half_rn(u[e] - __half2float(hi[e]));
-    part += __half2float(hi[e]) + __half2float(lo[e]);
-  }
+  // packed conversions: high = fp16(u), low = fp16(u - high)
+  const __half2 h01 = __floats2half2_rn(u[0], u[1]), h23 = __floats2half2_rn(u[2], u[3]);
+  const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+  const __half2 l01 = __floats2half2_rn(u[0] - f01.x, u[1] - f01.y);
+  const __half2 l23 = __floats2half2_rn(u[2] - f23.x, u[3] - f23.y);
+  // the sub-block sums feed only the Q4 min term: the fp32 values differ
+  // from high + low by at most 2^-22 relative
+  float part = (u[0] + u[1]) + (u[2] + u[3]);
   // k and k+1 (and k+2, k+3) are adjacent pairs in the permuted order
   const int p0 = act_perm(kl), p2 = act_perm(kl + 2);
   __half* chi = act + (2 * r) * cs2;
   __half* clo = act + (2 * r + 1) * cs2;
-  *reinterpret_cast<__half2*>(chi + p0) = __halves2half2(hi[0], hi[1]);
-  *reinterpret_cast<__half2*>(chi + p2) = __halves2half2(hi[2], hi[3]);
-  *reinterpret_cast<__half2*>(clo + p0) = __halves2half2(lo[0], lo[1]);
-  *reinterpret_cast<__half2*>(clo + p2) = __halves2half2(lo[2], lo[3]);
+  *reinterpret_cast<__half2*>(chi + p0) = h01;
+  *reinterpret_cast<__half2*>(chi + p2) = h23;
+  *reinterpret_cast<__half2*>(clo + p0) = l01;
+  *reinterpret_cast<__half2*>(clo + p2) = l23;
   // 8 consecutive threads hold one 32-wide sub-block
   part += __shfl_xor_sync(0xffffffffu, part, 1);
   part += __shfl_xor_sync(0xffffffffu, part, 2);
