@@ -885,37 +885,122 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
     // per-row gates and this task's 8 v values: [t] in shared memory after q, k
     float* vs = ks + kMaxT * 128;  // [kMaxT][8]
     float* gs = vs + kMaxT * 8;    // [kMaxT][2] alpha, beta
-#pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
-      if (t < T) {
-        float q4[4], k4[4];
-        float sq = 0.f, sk = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          q4[e] = k4[e] = 0.f;
-          if (e < ne) {
-            const int d = lane + 32 * e;
-            const bool own = qk_owner && d >= i0 && d < i0 + 8;
-            q4[e] = conv(g * dk + d, t, own);
-            k4[e] = conv(hk * dk + g * dk + d, t, own);
-            sq = fmaf(q4[e], q4[e], sq);
-            sk = fmaf(k4[e], k4[e], sk);
+    if (T == 1) {
+  #pragma unroll
+      for (int t = 0; t < kMaxT; ++t) {
+        if (t < T) {
+          float q4[4], k4[4];
+          float sq = 0.f, sk = 0.f;
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            q4[e] = k4[e] = 0.f;
+            if (e < ne) {
+              const int d = lane + 32 * e;
+              const bool own = qk_owner && d >= i0 && d < i0 + 8;
+              q4[e] = conv(g * dk + d, t, own);
+              k4[e] = conv(hk * dk + g * dk + d, t, own);
+              sq = fmaf(q4[e], q4[e], sq);
+              sk = fmaf(k4[e], k4[e], sk);
+            }
+          }
+          sq = warp_sum(sq);
+          sk = warp_sum(sk);
+          const float iq = 1.0f / sqrtf(sq + md.eps), ik = 1.0f / sqrtf(sk + md.eps);
+  #pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (e < ne) {
+              qs[t * 128 + lane + 32 * e] = q4[e] * iq;
+              ks[t * 128 + lane + 32 * e] = k4[e] * ik;
+            }
+          if (lane < 8) vs[t * 8 + lane] = conv(2 * hk * dk + h * dv + i0 + lane, t, true);
+          if (lane == 0) {
+            const float* yr = md.yin + static_cast<size_t>(row0 + t) * md.n_in_max;
+            gs[t * 2 + 0] = sigmoidf_(__ldcg(yr + a_off + h));
+            gs[t * 2 + 1] = sigmoidf_(__ldcg(yr + b_off + h));
           }
         }
-        sq = warp_sum(sq);
-        sk = warp_sum(sk);
-        const float iq = 1.0f / sqrtf(sq + md.eps), ik = 1.0f / sqrtf(sk + md.eps);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (e < ne) {
-            qs[t * 128 + lane + 32 * e] = q4[e] * iq;
-            ks[t * 128 + lane + 32 * e] = k4[e] * ik;
+      }
+    } else {
+      // T > 1: each channel's inputs are one sliding window over the history
+      // and the sequence's rows
+      const bool snap_rows = sd.seq_snap_all[si] != 0;
+      auto hist_store = [&](int ch, int t, float a, float b, float c) {
+        if (snap_rows || t == T - 1) {
+          const size_t ss = static_cast<size_t>(seq) * md.n_slots + sd.seq_slot_out[si][t];
+          float* ho = md.conv_state + (ss * md.n_gdn + gi) * 3 * C + ch;
+          __stcg(ho, a);
+          __stcg(ho + C, b);
+          __stcg(ho + 2 * C, c);
+        }
+      };
+      // each channel's inputs are loaded once as a sliding window over the
+      // history and the sequence's rows; every row's conv then comes from registers
+      float sq[kMaxT], sk[kMaxT];
+  #pragma unroll
+      for (int t = 0; t < kMaxT; ++t) sq[t] = sk[t] = 0.f;
+  #pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e < ne) {
+          const int d = lane + 32 * e;
+          const int chq = g * dk + d, chk = hk * dk + g * dk + d;
+          const bool own = qk_owner && d >= i0 && d < i0 + 8;
+          const float4 wq = *reinterpret_cast<const float4*>(cw + chq * 4);
+          const float4 wk = *reinterpret_cast<const float4*>(cw + chk * 4);
+          float xq[kMaxT + 3], xk[kMaxT + 3];
+  #pragma unroll
+          for (int j = 0; j < kMaxT + 3; ++j) {
+            xq[j] = xk[j] = 0.f;
+            if (j < T + 3) {
+              xq[j] = pre(chq, j - 3);
+              xk[j] = pre(chk, j - 3);
+            }
           }
-        if (lane < 8) vs[t * 8 + lane] = conv(2 * hk * dk + h * dv + i0 + lane, t, true);
-        if (lane == 0) {
-          const float* yr = md.yin + static_cast<size_t>(row0 + t) * md.n_in_max;
-          gs[t * 2 + 0] = sigmoidf_(__ldcg(yr + a_off + h));
-          gs[t * 2 + 1] = sigmoidf_(__ldcg(yr + b_off + h));
+  #pragma unroll
+          for (int t = 0; t < kMaxT; ++t) {
+            if (t < T) {
+              const float q = siluf_(fmaf(wq.w, xq[t + 3], fmaf(wq.z, xq[t + 2], fmaf(wq.y, xq[t + 1], wq.x * xq[t]))));
+              const float k = siluf_(fmaf(wk.w, xk[t + 3], fmaf(wk.z, xk[t + 2], fmaf(wk.y, xk[t + 1], wk.x * xk[t]))));
+              qs[t * 128 + d] = q;
+              ks[t * 128 + d] = k;
+              sq[t] = fmaf(q, q, sq[t]);
+              sk[t] = fmaf(k, k, sk[t]);
+              if (own) {
+                hist_store(chq, t, xq[t + 1], xq[t + 2], xq[t + 3]);
+                hist_store(chk, t, xk[t + 1], xk[t + 2], xk[t + 3]);
+              }
+            }
+          }
+        }
+      }
+      if (lane < 8) {
+        const int chv = 2 * hk * dk + h * dv + i0 + lane;
+        const float4 wv = *reinterpret_cast<const float4*>(cw + chv * 4);
+        float xv[kMaxT + 3];
+  #pragma unroll
+        for (int j = 0; j < kMaxT + 3; ++j) xv[j] = j < T + 3 ? pre(chv, j - 3) : 0.f;
+  #pragma unroll
+        for (int t = 0; t < kMaxT; ++t)
+          if (t < T) {
+            vs[t * 8 + lane] = siluf_(fmaf(wv.w, xv[t + 3], fmaf(wv.z, xv[t + 2], fmaf(wv.y, xv[t + 1], wv.x * xv[t]))));
+            hist_store(chv, t, xv[t + 1], xv[t + 2], xv[t + 3]);
+          }
+      }
+      if (lane < T) {
+        const float* yr = md.yin + static_cast<size_t>(row0 + lane) * md.n_in_max;
+        gs[lane * 2 + 0] = sigmoidf_(__ldcg(yr + a_off + h));
+        gs[lane * 2 + 1] = sigmoidf_(__ldcg(yr + b_off + h));
+      }
+      // L2 norms of q and k per row
+  #pragma unroll
+      for (int t = 0; t < kMaxT; ++t) {
+        if (t < T) {
+          const float iq = 1.0f / sqrtf(warp_sum(sq[t]) + md.eps), ik = 1.0f / sqrtf(warp_sum(sk[t]) + md.eps);
+  #pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (e < ne) {
+              qs[t * 128 + lane + 32 * e] *= iq;
+              ks[t * 128 + lane + 32 * e] *= ik;
+            }
         }
       }
     }
