@@ -31,6 +31,18 @@
  *   commit: L += kept rows; recurrent state <- snapshot after the last kept row;
  *     pages wholly beyond L are freed; new pages are the lowest free ids, in row
  *     order.
+ *   drafts for the next cycle (models with a multi-token-prediction block; the
+ *     page's "MTP catch-up rows for accepted tokens, then n_draft MTP draft
+ *     steps", restricted to the first draft_vocab tokens as its section "What
+ *     shipped" states): for each accepted row i = 0..a, whose next token is g_i,
+ *       m = W_fc [RMSNorm(h_i) w_h ; RMSNorm(emb(g_i)) w_e]    (h_i: the row's
+ *           final hidden state before the final norm)
+ *       m = one gated-attention decoder layer on m at position p_i, with its own
+ *           KV layer (index n_fa in the pool)
+ *       draft logits = W_lm[0:draft_vocab] RMSNorm_final'(m)
+ *     draft 1 = argmax of row a's draft logits; then for j = 1 .. n_draft-1 one
+ *     more pass with (previous pass's m, draft j) at position p_a + j gives
+ *     draft j+1.
  *
  * Every matrix-vector product sums over k in index order; threads split only
  * the output rows. Parity pins: tests/test_oracle_pins.py.
@@ -314,6 +326,11 @@ struct Seq {
     bool pending = false;
     int count = 0;
     std::vector<std::vector<double>> S_after, conv_after; /* per row */
+    /* Drafts of the last verify step (multi-token prediction), per draft pass:
+     * token, top-1 minus top-2 logit, rms of the logits, logits and the block's
+     * hidden output. */
+    std::vector<int> drafts;
+    std::vector<double> draft_gap, draft_rms, draft_logits, draft_hidden;
 };
 
 struct Oracle {
@@ -395,9 +412,22 @@ struct Oracle {
         for (int i = 0; i < qdim; ++i) out_o[i] = attn[i] * sigmoid(gate[i]);
     }
 
+    /* Feed-forward sub-layer with its residual: x += W_down (SiLU(W_gate u) (.) W_up u),
+     * u = RMSNorm(x) w_ffn. */
+    void feed_forward(const OrcLayerW& lw, double* x) {
+        const int H = L.hidden, F = L.ffn;
+        std::vector<double> u(H), y(H), g(F), up(F);
+        rmsnorm(x, lw.ffn_norm, H, L.eps, u.data());
+        q4_matvec(lw.w_gate, F, H, u.data(), g.data(), nthreads);
+        q4_matvec(lw.w_up, F, H, u.data(), up.data(), nthreads);
+        for (int i = 0; i < F; ++i) g[i] = silu(g[i]) * up[i];
+        q4_matvec(lw.w_down, H, F, g.data(), y.data(), nthreads);
+        for (int i = 0; i < H; ++i) x[i] += y[i];
+    }
+
     /* One row of the main model. Updates s (KV pool, S, conv); returns logits. */
     void forward_row(Seq& s, int token, int pos, double* logits, double* hidden_out) {
-        const int H = L.hidden, F = L.ffn;
+        const int H = L.hidden;
         std::vector<double> x(H), u(H), y(H);
         q4_row(W.embed, H, token, x.data());
         for (int l = 0; l < L.n_layers; ++l) {
@@ -442,19 +472,38 @@ struct Oracle {
                 q4_matvec(lw.w_o, H, L.hq * L.dh, o.data(), y.data(), nthreads);
             }
             for (int i = 0; i < H; ++i) x[i] += y[i];
-            /* feed-forward */
-            rmsnorm(x.data(), lw.ffn_norm, H, L.eps, u.data());
-            std::vector<double> g(F), up(F);
-            q4_matvec(lw.w_gate, F, H, u.data(), g.data(), nthreads);
-            q4_matvec(lw.w_up, F, H, u.data(), up.data(), nthreads);
-            for (int i = 0; i < F; ++i) g[i] = silu(g[i]) * up[i];
-            q4_matvec(lw.w_down, H, F, g.data(), y.data(), nthreads);
-            for (int i = 0; i < H; ++i) x[i] += y[i];
+            feed_forward(lw, x.data());
         }
         if (hidden_out) std::copy(x.begin(), x.end(), hidden_out);
         rmsnorm(x.data(), W.final_norm, H, L.eps, u.data());
         q4_matvec(lm(), L.vocab, H, u.data(), logits, nthreads);
     }
+
+    /* One row of the multi-token-prediction block: h is a final hidden state
+     * (before the final norm), next the token that follows it. Writes the
+     * block's KV at pos into the draft KV layer; returns the block's hidden
+     * output and the logits over the first draft_vocab tokens. */
+    void mtp_row(Seq& s, const double* h, int next, int pos, double* h_out, double* logits) {
+        const int H = L.hidden;
+        std::vector<double> cat(2 * static_cast<size_t>(H)), e(H), x(H), u(H), o(L.hq * L.dh), y(H);
+        rmsnorm(h, W.mtp_norm_h, H, L.eps, cat.data());
+        q4_row(W.embed, H, next, e.data());
+        rmsnorm(e.data(), W.mtp_norm_e, H, L.eps, cat.data() + H);
+        q4_matvec(W.mtp_fc, H, 2 * H, cat.data(), x.data(), nthreads);
+        rmsnorm(x.data(), W.mtp.attn_norm, H, L.eps, u.data());
+        attention_block(W.mtp, n_fa, s, pos, u.data(), o.data());
+        q4_matvec(W.mtp.w_o, H, L.hq * L.dh, o.data(), y.data(), nthreads);
+        for (int i = 0; i < H; ++i) x[i] += y[i];
+        feed_forward(W.mtp, x.data());
+        std::copy(x.begin(), x.end(), h_out);
+        rmsnorm(x.data(), W.mtp_final_norm, H, L.eps, u.data());
+        q4_matvec(lm(), L.draft_vocab, H, u.data(), logits, nthreads);
+    }
+
+    /* Drafts for the next cycle of a verified sequence: catch-up rows 0..a of
+     * this step (row i: hidden h_i, next token g_i, position p_i), then
+     * n_draft - 1 one-row passes chained on the block's own hidden output. */
+    void mtp_drafts(Seq& s, int a, const double* hidden, const int* g, const int* pos);
 
     void commit(Seq& s, int keep) {
         s.len += keep;
@@ -483,6 +532,37 @@ int argmax_lowest(const double* v, int n) {
     return best;
 }
 
+void Oracle::mtp_drafts(Seq& s, int a, const double* hidden, const int* g, const int* pos) {
+    const int H = L.hidden, DV = L.draft_vocab, n = L.n_draft;
+    std::vector<double> lg(DV), hin(H), hout(H);
+    s.drafts.assign(n, 0);
+    s.draft_gap.assign(n, 0.0);
+    s.draft_rms.assign(n, 0.0);
+    s.draft_logits.assign(static_cast<size_t>(n) * DV, 0.0);
+    s.draft_hidden.assign(static_cast<size_t>(n) * H, 0.0);
+    int token = -1;
+    for (int j = 0; j < n; ++j) {
+        if (j == 0) {
+            for (int i = 0; i <= a; ++i)
+                mtp_row(s, hidden + static_cast<size_t>(i) * H, g[i], pos[i], hout.data(), lg.data());
+        } else {
+            mtp_row(s, hin.data(), token, pos[a] + j, hout.data(), lg.data());
+        }
+        token = argmax_lowest(lg.data(), DV);
+        double second = -INFINITY, ss = 0;
+        for (int v = 0; v < DV; ++v) {
+            ss += lg[v] * lg[v];
+            if (v != token) second = std::max(second, lg[v]);
+        }
+        s.drafts[j] = token;
+        s.draft_gap[j] = lg[token] - second;
+        s.draft_rms[j] = std::sqrt(ss / DV);
+        std::copy(lg.begin(), lg.end(), s.draft_logits.begin() + static_cast<size_t>(j) * DV);
+        std::copy(hout.begin(), hout.end(), s.draft_hidden.begin() + static_cast<size_t>(j) * H);
+        hin = hout;
+    }
+}
+
 } /* namespace */
 
 extern "C" {
@@ -490,6 +570,7 @@ extern "C" {
 enum { ORC_OK = 0, ORC_INVALID = -1, ORC_NO_PAGES = -2 };
 
 void* orc_create(const OrcLayout* L, const OrcWeights* W, const OrcPool* P, int nthreads) {
+    if (L->has_mtp && (L->n_draft < 0 || L->draft_vocab < 1 || L->draft_vocab > L->vocab)) return nullptr;
     auto* o = new Oracle();
     o->L = *L;
     o->W = *W;
@@ -600,10 +681,16 @@ int orc_step(void* h, int n_rows, const int* tokens, const int* positions, const
         for (int j = 0; j < count[i]; ++j)
             if (positions[start[i] + j] != s.len + j) return ORC_INVALID;
     }
-    /* page allocation: lowest free id, in row order */
+    /* page allocation: lowest free id, in row order. With drafting, the last
+     * row of a verified sequence also reserves the positions its draft passes
+     * may write (up to its own position + n_draft - 1). */
+    const bool drafting = L.has_mtp && L.n_draft > 0;
     for (int r = 0; r < n_rows; ++r) {
         Seq& s = o->seqs[seq_ids[r]];
-        const int need = positions[r] / L.page_tokens + 1;
+        const bool last = r + 1 == n_rows || seq_ids[r + 1] != seq_ids[r];
+        const bool verify = !(flags && flags[r] != 0);
+        const int reach = positions[r] + (drafting && last && verify ? L.n_draft - 1 : 0);
+        const int need = reach / L.page_tokens + 1;
         while (static_cast<int>(s.pages.size()) < need) {
             if (o->free_pages.empty() || static_cast<int>(s.pages.size()) >= L.max_pages_per_seq)
                 return ORC_NO_PAGES;
@@ -658,8 +745,28 @@ int orc_step(void* h, int n_rows, const int* tokens, const int* positions, const
             out_counts[i] = a + 1;
             s.pending = true;
             s.count = a + 1;
+            if (drafting)
+                o->mtp_drafts(s, a, &o->last_hidden[static_cast<size_t>(start[i]) * L.hidden], &g[start[i]],
+                              &positions[start[i]]);
         }
     }
+    return ORC_OK;
+}
+
+/* Drafts computed by the last verify step of a sequence (models with a
+ * multi-token-prediction block): per draft pass its token, top-1 minus top-2
+ * draft logit, rms of the draft logits, the logits [n_draft][draft_vocab] and
+ * the block's hidden output [n_draft][hidden]. Pointers may be NULL. */
+int orc_drafts(void* h, int seq, int* drafts, double* gap, double* rms, double* logits, double* hidden) {
+    auto* o = static_cast<Oracle*>(h);
+    if (seq < 0 || seq >= o->L.max_seqs) return ORC_INVALID;
+    const Seq& s = o->seqs[seq];
+    if (s.drafts.empty()) return ORC_INVALID;
+    if (drafts) std::copy(s.drafts.begin(), s.drafts.end(), drafts);
+    if (gap) std::copy(s.draft_gap.begin(), s.draft_gap.end(), gap);
+    if (rms) std::copy(s.draft_rms.begin(), s.draft_rms.end(), rms);
+    if (logits) std::copy(s.draft_logits.begin(), s.draft_logits.end(), logits);
+    if (hidden) std::copy(s.draft_hidden.begin(), s.draft_hidden.end(), hidden);
     return ORC_OK;
 }
 

@@ -74,6 +74,7 @@ def lib():
         L.orc_seq_get.argtypes = [vp, i32, vp, vp, vp, vp, vp]
         L.orc_commit.argtypes = [vp, i32, vp, vp]
         L.orc_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_drafts.argtypes = [vp, i32, vp, vp, vp, vp, vp]
         L.orc_q4_decode.argtypes = [vp, i64, vp]
         L.orc_q4_encode.argtypes = [vp, i64, vp]
         L.orc_q4_matvec.argtypes = [vp, i32, i32, vp, vp, i32]
@@ -92,7 +93,7 @@ def lib():
         L.orc_silu.argtypes = [dbl]
         L.orc_silu.restype = dbl
         L.orc_n_free_pages.argtypes = [vp]
-        for f in ("orc_seq_set", "orc_seq_get", "orc_commit", "orc_step", "orc_n_free_pages"):
+        for f in ("orc_seq_set", "orc_seq_get", "orc_commit", "orc_step", "orc_n_free_pages", "orc_drafts"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -153,6 +154,8 @@ class Oracle:
         self.W, self.P = W, P
         self.nthreads = int(nthreads or os.cpu_count() or 1)
         self.h = lib().orc_create(ctypes.byref(self.L), ctypes.byref(W), ctypes.byref(P), self.nthreads)
+        if not self.h:
+            raise ValueError("orc_create rejected the layout")
 
     def __del__(self):
         if getattr(self, "h", None):
@@ -217,6 +220,20 @@ class Oracle:
         n_out = int(out_counts.sum())
         return dict(tokens=out_tokens[:n_out], counts=out_counts, logits=logits, hidden=hidden,
                     argmax=argmax, gap=gap, rms=rms)
+
+    def drafts(self, seq: int):
+        """Drafts of the sequence's last verify step (model with a
+        multi-token-prediction block and n_draft > 0)."""
+        m, n = self.model, self.L.n_draft
+        d = np.zeros(n, np.int32)
+        gap = np.zeros(n, np.float64)
+        rms = np.zeros(n, np.float64)
+        logits = np.zeros((n, m["draft_vocab"]), np.float64)
+        hidden = np.zeros((n, m["hidden"]), np.float64)
+        rc = lib().orc_drafts(self.h, seq, _p(d), _p(gap), _p(rms), _p(logits), _p(hidden))
+        if rc:
+            raise ValueError(f"orc_drafts failed ({rc})")
+        return dict(tokens=d, gap=gap, rms=rms, logits=logits, hidden=hidden)
 
     def n_free_pages(self):
         return lib().orc_n_free_pages(self.h)
