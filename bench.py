@@ -65,23 +65,31 @@ def measured_traffic(algorithmic):
         return None
 
 
-def algorithmic_bytes(model, kv_q8, seqs):
+def algorithmic_bytes(model, kv_q8, seqs, n_draft=0):
     """Bytes the step must move: every streamed weight once, the embedding rows
     it gathers, each sequence's cached K/V once per attention layer plus the
-    new rows, and the recurrent state read once and written once."""
+    new rows, and the recurrent state read once and written once. With an MTP
+    head, each of its n_draft sequential passes streams the head's weights and
+    the lm_head rows of the draft vocabulary again, gathers embedding rows,
+    and reads the head's KV layer."""
     from gen.configs import model_dims, tensor_inventory
     d = model_dims(model)
     R = sum(T for _c, T in seqs)
+    H = model["hidden"]
+    passes = n_draft if model.get("has_mtp") else 0
     w = 0.0
     for name, _tid, kind, shape in tensor_inventory(model):
         if kind != "q4":
             continue
         if name == "embed" and not model["tied"]:
             continue
-        w += shape[0] * shape[1] * 0.5625
-    w += R * model["hidden"] * 0.5625
-    per_tok = d["n_fa"] * model["hkv"] * model["dh"] * 2 * ((1 + 2 / 32) if kv_q8 else 2)
+        w += shape[0] * shape[1] * 0.5625 * (passes if name.startswith("mtp.") else 1)
+    w += R * H * 0.5625
+    w += passes * (model.get("draft_vocab", 0) * H + R * H) * 0.5625
+    per_layer = model["hkv"] * model["dh"] * 2 * ((1 + 2 / 32) if kv_q8 else 2)
+    per_tok = d["n_fa"] * per_layer
     kv = sum(c for c, _T in seqs) * per_tok + R * per_tok
+    kv += passes * (sum(c for c, _T in seqs) + R) * per_layer
     nseq = len(seqs)
     state = nseq * 2 * d["n_gdn"] * model["hv"] * model["dv"] * model["dk"] * 4
     conv = nseq * 2 * d["n_gdn"] * (model["conv_w"] - 1) * d["conv_ch"] * 4
@@ -169,7 +177,9 @@ def cpu_oracle_sample(workload, budget_s=20.0):
     from oracle import oracle as orc
     nthreads = os.cpu_count() or 1
     wl = Workload(workload, nthreads=nthreads)
-    o = orc.Oracle(wl.model, wl.weights, wl.pool, wl.kv_q8, wl.n_pages, wl.max_seqs, nthreads=nthreads)
+    n_draft = int(wl.spec.get("n_draft", 0)) if wl.model.get("has_mtp") else 0
+    o = orc.Oracle(wl.model, wl.weights, wl.pool, wl.kv_q8, wl.n_pages, wl.max_seqs, nthreads=nthreads,
+                   n_draft=n_draft)
     for s, (cached, _T) in enumerate(wl.seqs):
         o.seq_set(s, cached, wl.tables[s], *wl.states[s])
     tok, pos, sid = wl.rows()
@@ -228,7 +238,9 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     t_setup = time.perf_counter()
     wl = Workload(args.workload, nthreads=os.cpu_count(), overrides=layer_override(args))
-    eng = mk.Engine(wl.model, wl.weights, wl.kv_q8, wl.n_pages, max_seqs=wl.max_seqs, device=f"cuda:{local}")
+    n_draft = int(wl.spec.get("n_draft", 0)) if wl.model.get("has_mtp") else 0
+    eng = mk.Engine(wl.model, wl.weights, wl.kv_q8, wl.n_pages, max_seqs=wl.max_seqs, device=f"cuda:{local}",
+                    n_draft=n_draft)
     eng.load_pool(wl.pool)
     for s, (cached, _T) in enumerate(wl.seqs):
         eng.seq_set(s, cached, wl.tables[s], *wl.states[s])
@@ -286,7 +298,7 @@ def run_ours(args, world, rank, local):
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(world, e2e_s, dev)
 
-    ab = algorithmic_bytes(wl.model, wl.kv_q8, wl.seqs)
+    ab = algorithmic_bytes(wl.model, wl.kv_q8, wl.seqs, n_draft)
     peak, peak_kind = peaks()
     launch_ms = statistics.median(per_launch) if per_launch else ms
     achieved = ab["total"] / (launch_ms * 1e-3) / 1e9

@@ -76,8 +76,8 @@ typedef struct mk_layout {
     float rope_base;
     int32_t gdn_hk, gdn_hv, gdn_dk, gdn_dv, conv_w;
     int32_t tied_lm_head;  /* 1: logits use the embedding matrix */
-    int32_t has_mtp;       /* reserved: multi-token-prediction head (must be 0 in this build) */
-    int32_t draft_vocab;   /* reserved */
+    int32_t has_mtp;       /* 1: the model has a multi-token-prediction (MTP) draft head */
+    int32_t draft_vocab;   /* MTP drafts are argmax over vocabulary rows [0, draft_vocab) */
     int32_t kv_dtype;      /* MK_KV_F16 or MK_KV_Q8 */
     int32_t page_tokens;   /* tokens per KV page (16) */
     int32_t n_pages;       /* pages in the pool */
@@ -85,6 +85,7 @@ typedef struct mk_layout {
     int32_t max_pages_per_seq;
     int32_t n_state_slots; /* recurrent-state slots per sequence, >= MK_MAX_T + 1 */
     float rms_eps;         /* RMSNorm and L2-norm epsilon (1e-6) */
+    int32_t n_draft;       /* MTP: drafts made per verified sequence and step, 1..MK_MAX_T-1 */
 } mk_layout;
 
 /* Canonical weights of one layer. Q4 matrices are [rows][k/256] super-blocks
@@ -112,20 +113,30 @@ typedef struct mk_layer_weights {
     const void* w_down;      /* [hidden][ffn] Q4 */
 } mk_layer_weights;
 
+/* The MTP draft head (used when has_mtp): m = W_fc [RMSNorm(h) norm_h ;
+ * RMSNorm(embed(next token)) norm_e], one gated-attention decoder layer on m
+ * (its own KV layer, the last one of the pool), then RMSNorm(m) final_norm
+ * and the lm_head rows [0, draft_vocab). */
 typedef struct mk_weights {
     const void* embed;       /* [vocab][hidden] Q4 */
     const float* final_norm; /* [hidden] */
     const void* lm_head;     /* [vocab][hidden] Q4, NULL when tied_lm_head */
     mk_layer_weights layers[MK_MAX_LAYERS];
+    mk_layer_weights mtp;        /* MTP block: the gated-attention fields */
+    const void* mtp_fc;          /* [hidden][2*hidden] Q4 */
+    const float* mtp_norm_h;     /* [hidden] */
+    const float* mtp_norm_e;     /* [hidden] */
+    const float* mtp_final_norm; /* [hidden] */
 } mk_weights;
 
 /* Device buffers the caller allocates (sizes from the mk_*_bytes queries). */
 typedef struct mk_buffers {
     void* packed;            /* mk_packed_bytes(): written once by mk_create */
-    /* KV pool, one attention layer after another:
-     *   F16: k, v   = binary16 [n_fa][n_pages][fa_hkv][page_tokens][fa_dh]
+    /* KV pool, one attention layer after another (n_kv = number of gated
+     * attention layers, plus one for the MTP block when has_mtp):
+     *   F16: k, v   = binary16 [n_kv][n_pages][fa_hkv][page_tokens][fa_dh]
      *   Q8 : k, v   = int8 codes, same shape
-     *        k_scale, v_scale = binary16 [n_fa][n_pages][fa_hkv][page_tokens][fa_dh/32] */
+     *        k_scale, v_scale = binary16 [n_kv][n_pages][fa_hkv][page_tokens][fa_dh/32] */
     void* kv_k;
     void* kv_v;
     void* kv_k_scale;
@@ -190,7 +201,9 @@ mk_status mk_seq_get(mk_ctx* ctx, int32_t seq, int32_t* length, int32_t* pages,
  * row_flags may be NULL (all 0); 0 = verify row. A sequence may appear once.
  * Before the launch the library commits any pending step of the sequences in
  * this step (keeping every accepted row) and allocates pages for the new
- * positions: the lowest free page id first, in row order.
+ * positions: the lowest free page id first, in row order. With an MTP head
+ * the last row of each sequence also reserves the positions its draft passes
+ * may write (up to its position + n_draft - 1).
  * Outputs (host): out_tokens[n_rows] receives, per sequence in order of
  * first appearance, the accepted drafts followed by the bonus token (the
  * main model's greedy choice after the last accepted row); out_counts[number
@@ -216,6 +229,20 @@ mk_status mk_step_prepare(mk_ctx* ctx, int32_t n_rows, const int32_t* tokens,
                           const uint8_t* row_flags);
 mk_status mk_step_launch(mk_ctx* ctx);
 mk_status mk_step_finish(mk_ctx* ctx, int32_t* out_tokens, int32_t* out_counts);
+
+/*
+ * Drafts the MTP head made in the same launch as the last completed step
+ * ("Fusing the whole speculative-decoding cycle into one CUDA kernel", section
+ * "What shipped": catch-up rows for the accepted tokens, then n_draft draft
+ * steps). drafts (host) receives [sequences of that step, in their order]
+ * [n_draft]: for each sequence, catch-up over its accepted rows i = 0..a (row
+ * i's final hidden state with the embedding of its greedy token, at its
+ * position) gives draft 1 from row a; draft j+1 comes from one more pass on
+ * draft j and the head's previous hidden output at position p_a + j. They
+ * are the drafts of the sequence's next step when it keeps all accepted rows.
+ * Errors: MK_ERR_INVALID (no MTP head, or no completed step).
+ */
+mk_status mk_last_drafts(mk_ctx* ctx, int32_t* drafts);
 
 /*
  * Keep n_keep[i] rows (1 <= n_keep[i] <= count of its last step) of each
@@ -244,7 +271,8 @@ mk_status mk_debug_scratch(mk_ctx* ctx, int32_t rows, float* x, float* y, float*
  * 5*n_layers + 4 uint64 values, every following launch writes the
  * %globaltimer value (ns) at its start and when block 0 leaves the grid
  * barrier closing each phase (embed, then per layer: input GEMM, mixer,
- * o_proj, gate/up, down; then lm_head; then verify). NULL stops it. */
+ * o_proj, gate/up, down; then lm_head; then verify; an MTP head's draft
+ * passes after verify are not stamped). NULL stops it. */
 mk_status mk_debug_timeline(mk_ctx* ctx, uint64_t* stamps);
 
 /* Device-side timing of the last mk_step_launch in milliseconds (CUDA events
@@ -278,7 +306,7 @@ int32_t mk_grid_blocks(mk_ctx* ctx);
  * call; the context itself must already exist (mk_create allocates).
  *  - Sizes: a context whose worst-case step scratch exceeds 16 MiB is refused
  *    with MK_ERR_UNSUPPORTED before any bookkeeping changes (small models
- *    fit; the 27B-shaped model does not).
+ *    fit; the 27B-shaped model does not). So is a model with an MTP head.
  *  - The first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress; make that first call before any stream capture.
  *  - Every call shares the one array and it keeps the previous call's

@@ -41,10 +41,13 @@ struct PhasePlan {
 struct Plan {
   bool ok = false;
   int n_gdn = 0, n_fa = 0, conv_ch = 0, n_in_gdn = 0, n_in_fa = 0, n_in_max = 0, o_stride = 0;
-  PhasePlan in[MK_MAX_LAYERS], o[MK_MAX_LAYERS], gu[MK_MAX_LAYERS], down[MK_MAX_LAYERS], lm;
+  // index MK_MAX_LAYERS holds the MTP block
+  PhasePlan in[MK_MAX_LAYERS + 1], o[MK_MAX_LAYERS + 1], gu[MK_MAX_LAYERS + 1], down[MK_MAX_LAYERS + 1], lm;
+  PhasePlan mtp_fc;
   size_t off_embed = 0;
-  size_t off_attn_norm[MK_MAX_LAYERS], off_ffn_norm[MK_MAX_LAYERS], off_conv[MK_MAX_LAYERS],
+  size_t off_attn_norm[MK_MAX_LAYERS + 1], off_ffn_norm[MK_MAX_LAYERS + 1], off_conv[MK_MAX_LAYERS],
       off_onorm[MK_MAX_LAYERS], off_final_norm = 0;
+  size_t off_mtp_norm_h = 0, off_mtp_norm_e = 0, off_mtp_final_norm = 0;
   size_t total = 0;
 };
 
@@ -57,7 +60,7 @@ bool layout_ok(const mk_layout& L) {
     else if (L.layer_kind[l] == MK_LAYER_GDN) has_gdn = true;
     else return false;
   }
-  if (has_fa) {
+  if (has_fa || L.has_mtp) {  // the MTP block is a gated-attention layer
     if (L.fa_hq <= 0 || L.fa_hkv <= 0 || L.fa_hq % L.fa_hkv) return false;
     if (L.fa_dh <= 0 || L.fa_dh % 64 || L.fa_dh > kMaxDh) return false;
     if ((L.fa_hq * L.fa_dh) % 256) return false;
@@ -70,7 +73,10 @@ bool layout_ok(const mk_layout& L) {
     if (256 % L.gdn_dv) return false;
     if (L.conv_w != 4) return false;
   }
-  if (L.has_mtp) return false;
+  if (L.has_mtp) {
+    if (L.n_draft < 1 || L.n_draft > kMaxDraft) return false;
+    if (L.draft_vocab < 1 || L.draft_vocab > L.vocab) return false;
+  }
   if (L.kv_dtype != MK_KV_F16 && L.kv_dtype != MK_KV_Q8) return false;
   if (L.page_tokens != 16 || L.n_pages <= 0) return false;
   if (L.max_seqs <= 0 || L.max_seqs > MK_MAX_SEQS || L.max_pages_per_seq <= 0) return false;
@@ -107,6 +113,16 @@ Plan make_plan(const mk_layout& L) {
     phase(p.down[l], H, F);
   }
   phase(p.lm, L.vocab, H);
+  if (L.has_mtp) {
+    const int M = MK_MAX_LAYERS;
+    phase(p.mtp_fc, H, 2 * H);
+    phase(p.in[M], p.n_in_fa, H);
+    phase(p.o[M], H, L.fa_hq * L.fa_dh);
+    phase(p.gu[M], 2 * F, H);
+    phase(p.down[M], H, F);
+    p.n_in_max = std::max(p.n_in_max, p.n_in_fa);
+    p.o_stride = std::max(p.o_stride, L.fa_hq * L.fa_dh);
+  }
   p.n_in_max = tiles_of(p.n_in_max) * kTileRows;
   p.off_embed = at;
   at = align_up(at + q4_bytes(L.vocab, H));
@@ -120,6 +136,14 @@ Plan make_plan(const mk_layout& L) {
   }
   p.off_final_norm = at;
   at = align_up(at + H * 4);
+  if (L.has_mtp) {
+    const int M = MK_MAX_LAYERS;
+    p.off_attn_norm[M] = at; at = align_up(at + H * 4);
+    p.off_ffn_norm[M] = at; at = align_up(at + H * 4);
+    p.off_mtp_norm_h = at; at = align_up(at + H * 4);
+    p.off_mtp_norm_e = at; at = align_up(at + H * 4);
+    p.off_mtp_final_norm = at; at = align_up(at + H * 4);
+  }
   p.total = at;
   p.ok = true;
   return p;
@@ -156,6 +180,7 @@ struct SeqInfo {
 
 struct mk_ctx {
   mk_layout L;
+  std::vector<int32_t> drafts;  // [sequences of the last completed step][n_draft]
   Plan plan;
   cudaStream_t stream = nullptr;
   int grid = 0;
@@ -166,6 +191,7 @@ struct mk_ctx {
   int32_t* out_host = nullptr;  // pinned [kOutInts + 4]
   int32_t* pt_host = nullptr;   // pinned page-table mirror
   float* attn_scratch = nullptr;
+  double* inv_freq = nullptr;  // device [kMaxDh/2]
   CUtensorMap tm_k{}, tm_v{};  // 2-D tensor maps of the K and V pools (attention page copies)
   std::vector<void*> allocs;
   std::vector<SeqInfo> seqs;
@@ -238,15 +264,18 @@ static int n_fa_of(const mk_layout* L) {
   return n;
 }
 
+// KV layers of the pool: one per gated-attention layer, plus the MTP block's.
+static int n_kv_of(const mk_layout* L) { return n_fa_of(L) + (L->has_mtp ? 1 : 0); }
+
 size_t mk_kv_bytes(const mk_layout* L) {
   if (!L || !layout_ok(*L)) return 0;
-  const size_t elems = static_cast<size_t>(n_fa_of(L)) * L->n_pages * L->fa_hkv * L->page_tokens * L->fa_dh;
+  const size_t elems = static_cast<size_t>(n_kv_of(L)) * L->n_pages * L->fa_hkv * L->page_tokens * L->fa_dh;
   return elems * (L->kv_dtype == MK_KV_Q8 ? 1 : 2);
 }
 
 size_t mk_kv_scale_bytes(const mk_layout* L) {
   if (!L || !layout_ok(*L) || L->kv_dtype != MK_KV_Q8) return 0;
-  return static_cast<size_t>(n_fa_of(L)) * L->n_pages * L->fa_hkv * L->page_tokens * (L->fa_dh / 32) * 2;
+  return static_cast<size_t>(n_kv_of(L)) * L->n_pages * L->fa_hkv * L->page_tokens * (L->fa_dh / 32) * 2;
 }
 
 size_t mk_gdn_state_bytes(const mk_layout* L) {
@@ -392,6 +421,44 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
     ok = ok && cudaMemcpyAsync(packed + p.off_final_norm, w->final_norm, H * 4, cudaMemcpyDeviceToDevice, c->stream) == cudaSuccess;
   }
   if (!ok) { mk_free(c); return MK_ERR_CUDA; }
+  if (L.has_mtp) {
+    const mk_layer_weights& mw = w->mtp;
+    const int M = MK_MAX_LAYERS;
+    if (!w->mtp_fc || !w->mtp_norm_h || !w->mtp_norm_e || !w->mtp_final_norm || !mw.w_q || !mw.w_g || !mw.w_k ||
+        !mw.w_v || !mw.w_o || !mw.w_gate || !mw.w_up || !mw.w_down || !mw.attn_norm || !mw.ffn_norm) {
+      mk_free(c);
+      return MK_ERR_INVALID;
+    }
+    const int qd = L.fa_hq * L.fa_dh, kd = L.fa_hkv * L.fa_dh;
+    PackSrc sf{};
+    sf.n_seg = 1; sf.row_begin[0] = 0; sf.row_end[0] = H; sf.src[0] = static_cast<const uint8_t*>(w->mtp_fc);
+    ok = pack(p.mtp_fc, sf);
+    PackSrc s{};
+    s.n_seg = 4;
+    s.row_begin[0] = 0; s.row_end[0] = qd; s.src[0] = static_cast<const uint8_t*>(mw.w_q);
+    s.row_begin[1] = qd; s.row_end[1] = 2 * qd; s.src[1] = static_cast<const uint8_t*>(mw.w_g);
+    s.row_begin[2] = 2 * qd; s.row_end[2] = 2 * qd + kd; s.src[2] = static_cast<const uint8_t*>(mw.w_k);
+    s.row_begin[3] = 2 * qd + kd; s.row_end[3] = 2 * qd + 2 * kd; s.src[3] = static_cast<const uint8_t*>(mw.w_v);
+    ok = ok && pack(p.in[M], s);
+    PackSrc so{};
+    so.n_seg = 1; so.row_begin[0] = 0; so.row_end[0] = H; so.src[0] = static_cast<const uint8_t*>(mw.w_o);
+    ok = ok && pack(p.o[M], so);
+    PackSrc sg{};
+    sg.n_seg = 2; sg.interleave_gate_up = 1;
+    sg.row_begin[0] = 0; sg.row_end[0] = F; sg.src[0] = static_cast<const uint8_t*>(mw.w_gate);
+    sg.row_begin[1] = 0; sg.row_end[1] = F; sg.src[1] = static_cast<const uint8_t*>(mw.w_up);
+    ok = ok && pack(p.gu[M], sg);
+    PackSrc sd{};
+    sd.n_seg = 1; sd.row_begin[0] = 0; sd.row_end[0] = H; sd.src[0] = static_cast<const uint8_t*>(mw.w_down);
+    ok = ok && pack(p.down[M], sd);
+    auto vec = [&](size_t off, const float* src) {
+      return cudaMemcpyAsync(packed + off, src, H * 4, cudaMemcpyDeviceToDevice, c->stream) == cudaSuccess;
+    };
+    ok = ok && vec(p.off_attn_norm[M], mw.attn_norm) && vec(p.off_ffn_norm[M], mw.ffn_norm) &&
+         vec(p.off_mtp_norm_h, w->mtp_norm_h) && vec(p.off_mtp_norm_e, w->mtp_norm_e) &&
+         vec(p.off_mtp_final_norm, w->mtp_final_norm);
+    if (!ok) { mk_free(c); return MK_ERR_CUDA; }
+  }
 
   // ---- launch geometry
   int bps = 0;
@@ -437,6 +504,33 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
     ld.conv_w = gdn ? reinterpret_cast<const float*>(packed + p.off_conv[l]) : nullptr;
   }
   gemm(md.lm, p.lm, PRO_RMS_X, EPI_TOP2, reinterpret_cast<const float*>(packed + p.off_final_norm));
+  md.lm.dump = 1;
+  if (L.has_mtp) {
+    // the MTP block is layer n_layers: a gated-attention layer on KV layer n_fa
+    const int M = MK_MAX_LAYERS;
+    LayerDesc& ld = md.layer[L.n_layers];
+    ld.kind = MK_LAYER_FA;
+    ld.gdn_i = -1;
+    ld.fa_i = fi;
+    gemm(ld.in, p.in[M], PRO_RMS_X, EPI_STORE_YIN, reinterpret_cast<const float*>(packed + p.off_attn_norm[M]));
+    gemm(ld.o, p.o[M], PRO_FA_OUT, EPI_RESID_X, nullptr);
+    gemm(ld.gu, p.gu[M], PRO_RMS_X, EPI_STORE_GU, reinterpret_cast<const float*>(packed + p.off_ffn_norm[M]));
+    gemm(ld.down, p.down[M], PRO_H, EPI_RESID_X, nullptr);
+    ld.o.zero_buf = ZERO_GU;
+    ld.down.zero_buf = ZERO_YIN;
+    ld.conv_w = nullptr;
+    gemm(md.mtp_fc, p.mtp_fc, PRO_MTP_IN, EPI_RESID_X, nullptr);
+    // the draft lm_head is the first tiles of the packed lm_head (rows [0, draft_vocab))
+    PhasePlan dl = p.lm;
+    dl.n_tiles = tiles_of(L.draft_vocab);
+    dl.n_out = L.draft_vocab;
+    gemm(md.mtp_lm, dl, PRO_RMS_X, EPI_TOP2, reinterpret_cast<const float*>(packed + p.off_mtp_final_norm));
+    md.has_mtp = 1;
+    md.n_draft = L.n_draft;
+    md.draft_vocab = L.draft_vocab;
+    md.mtp_norm_h = reinterpret_cast<const float*>(packed + p.off_mtp_norm_h);
+    md.mtp_norm_e = reinterpret_cast<const float*>(packed + p.off_mtp_norm_e);
+  }
   // split tiles are summed into buffers that must start at zero: the
   // gate/up sums are cleared during o_proj, the next input projections during down
   for (int l = 0; l < L.n_layers; ++l) {
@@ -459,7 +553,8 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   md.max_seg = max_seg;
   md.kv_k = b->kv_k; md.kv_v = b->kv_v;
   md.kv_ks = static_cast<uint16_t*>(b->kv_k_scale); md.kv_vs = static_cast<uint16_t*>(b->kv_v_scale);
-  if (p.n_fa > 0 && (!encode_kv_map(&c->tm_k, b->kv_k, L, p.n_fa) || !encode_kv_map(&c->tm_v, b->kv_v, L, p.n_fa))) {
+  const int n_kv = n_kv_of(&L);
+  if (n_kv > 0 && (!encode_kv_map(&c->tm_k, b->kv_k, L, n_kv) || !encode_kv_map(&c->tm_v, b->kv_v, L, n_kv))) {
     mk_free(c);
     return MK_ERR_CUDA;
   }
@@ -491,6 +586,11 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
       (e = dev_alloc(c, &md.bar, 64)) ||
       (e = dev_alloc(c, &md.err, 64)) ||
       (e = dev_alloc(c, &c->attn_scratch, nrec * 2 * kMaxDh * 4)) ||
+      (e = dev_alloc(c, &md.mtp_in, L.has_mtp ? static_cast<size_t>(kMaxRows) * 2 * H * 4 : 0)) ||
+      (e = dev_alloc(c, &md.mtp_h, L.has_mtp ? static_cast<size_t>(kMaxSeqs) * H * 4 : 0)) ||
+      (e = dev_alloc(c, &md.mtp_rope, static_cast<size_t>(kMaxSeqs) * (kMaxDh / 2) * sizeof(float2))) ||
+      (e = dev_alloc(c, &md.mtp_row, static_cast<size_t>(kMaxSeqs) * 2 * 4)) ||
+      (e = dev_alloc(c, &c->inv_freq, (kMaxDh / 2) * sizeof(double))) ||
       (e = dev_alloc(c, &c->md_dev, sizeof(ModelDesc))) ||
       (e = dev_alloc(c, &c->sd_dev, sizeof(StepDesc)))) {
     mk_free(c);
@@ -503,7 +603,13 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
     mk_free(c);
     return MK_ERR_CUDA;
   }
-  if (cudaMemcpyAsync(c->md_dev, &md, sizeof(ModelDesc), cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
+  // RoPE inverse frequencies in double, for the angles the draft passes compute on the device
+  double inv_freq[kMaxDh / 2] = {0.0};
+  for (int i = 0; i < L.fa_dh / 2; ++i)
+    inv_freq[i] = std::pow(static_cast<double>(L.rope_base), -2.0 * i / std::max(1, L.fa_dh));
+  md.inv_freq = c->inv_freq;
+  if (cudaMemcpyAsync(c->inv_freq, inv_freq, sizeof(inv_freq), cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
+      cudaMemcpyAsync(c->md_dev, &md, sizeof(ModelDesc), cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
       cudaStreamSynchronize(c->stream) != cudaSuccess) {
     mk_free(c);
     return MK_ERR_CUDA;
@@ -642,13 +748,16 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
   for (int i = 0; i < n_seq; ++i) {
     if (T[i] > kMaxT || T[i] + 1 > L.n_state_slots || T[i] * grp > kMaxQRows) return MK_ERR_UNSUPPORTED;
   }
+  // positions the step may write per sequence beyond its rows: the MTP draft
+  // passes after the last row
+  const int extra = L.has_mtp ? L.n_draft - 1 : 0;
   // positions must continue each sequence (after its pending step is kept)
   for (int i = 0; i < n_seq; ++i) {
     const SeqInfo& s = c->seqs[sid[i]];
     const int base = s.len + (s.pending ? s.count : 0);
     for (int j = 0; j < T[i]; ++j)
       if (positions[row0[i] + j] != base + j) return MK_ERR_INVALID;
-    if ((base + T[i] + L.page_tokens - 1) / L.page_tokens > L.max_pages_per_seq) return MK_ERR_NO_PAGES;
+    if ((base + T[i] + extra + L.page_tokens - 1) / L.page_tokens > L.max_pages_per_seq) return MK_ERR_NO_PAGES;
   }
   // page demand check before touching any state: pages a pending step does
   // not keep are released by its auto-commit first
@@ -662,7 +771,7 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
         const int keep = (len_after + L.page_tokens - 1) / L.page_tokens;
         if (have > keep) { released += have - keep; have = keep; }
       }
-      const int want = (len_after + T[i] + L.page_tokens - 1) / L.page_tokens;
+      const int want = (len_after + T[i] + extra + L.page_tokens - 1) / L.page_tokens;
       need += std::max(0, want - have);
     }
     if (need > static_cast<int>(c->free_pages.size()) + released) return MK_ERR_NO_PAGES;
@@ -672,10 +781,12 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
     SeqInfo& s = c->seqs[sid[i]];
     if (s.pending) commit_seq(c, s, s.count);
   }
-  // page allocation, lowest free first, in row order
+  // page allocation, lowest free first, in row order (a sequence's last row
+  // also covers its draft passes' positions)
   for (int r = 0; r < n_rows; ++r) {
     SeqInfo& s = c->seqs[seq_ids[r]];
-    const int need = positions[r] / L.page_tokens + 1;
+    const bool last = r + 1 == n_rows || seq_ids[r + 1] != seq_ids[r];
+    const int need = (positions[r] + (last ? extra : 0)) / L.page_tokens + 1;
     while (static_cast<int>(s.pages.size()) < need) {
       if (c->free_pages.empty()) return MK_ERR_NO_PAGES;
       s.pages.push_back(*c->free_pages.begin());
@@ -788,6 +899,7 @@ mk_status mk_step_launch(mk_ctx* c) {
 
 mk_status mk_step_finish(mk_ctx* c, int32_t* out_tokens, int32_t* out_counts) {
   if (!c || !c->launched) return MK_ERR_INVALID;
+  c->drafts.clear();
   int32_t* h = c->out_host;
   if (cudaMemcpyAsync(h, c->md_host.out, kOutInts * 4, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
       cudaMemcpyAsync(h + kOutInts, c->md_host.err, 16, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
@@ -805,6 +917,9 @@ mk_status mk_step_finish(mk_ctx* c, int32_t* out_tokens, int32_t* out_counts) {
     return MK_ERR_BARRIER_TIMEOUT;
   }
   int at = 0;
+  if (c->L.has_mtp)
+    for (int i = 0; i < c->n_seq; ++i)
+      for (int j = 0; j < c->L.n_draft; ++j) c->drafts.push_back(h[kOutDrafts + i * kMaxDraft + j]);
   for (int i = 0; i < c->n_seq; ++i) {
     const int cnt = h[kOutCounts + i];
     if (cnt < 1 || cnt > c->step_T[i]) return MK_ERR_CUDA;
@@ -828,6 +943,12 @@ mk_status mk_step(mk_ctx* c, int32_t n_rows, const int32_t* tokens, const int32_
   s = mk_step_launch(c);
   if (s != MK_OK) return s;
   return mk_step_finish(c, out_tokens, out_counts);
+}
+
+mk_status mk_last_drafts(mk_ctx* c, int32_t* drafts) {
+  if (!c || !drafts || !c->L.has_mtp || c->drafts.empty()) return MK_ERR_INVALID;
+  std::copy(c->drafts.begin(), c->drafts.end(), drafts);
+  return MK_OK;
 }
 
 float mk_last_launch_ms(mk_ctx* c) {
@@ -896,6 +1017,7 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
                                     const int32_t* seq_ids, const uint8_t* row_flags, int32_t* out_tokens,
                                     int32_t* out_counts) {
   if (!c) return MK_ERR_INVALID;
+  if (c->L.has_mtp) return MK_ERR_UNSUPPORTED;
   // The worst case of this context (every attention item a step can have)
   // must fit, so that the check happens before any bookkeeping changes.
   const int worst_items = c->grid + kMaxSeqs * std::max(1, c->L.fa_hkv);

@@ -63,9 +63,14 @@ constexpr int kChunk = 16;                    // cached tokens per attention chu
 constexpr int kPartStride = kMaxDh + 4;       // floats per query row of a split partial: dims, m, l, pad
 constexpr int kAttnMaxSlots = 16;             // KV staging slots (their mbarriers live in misc)
 constexpr int kAttnBarOff = 3840;             // byte offset of those mbarriers inside misc
+constexpr int kMaxDraft = MK_MAX_T - 1;       // MTP drafts per sequence and step
+// the step's own rows plus the draft passes' positions fit one new-rows chunk
+static_assert(kMaxT + kMaxDraft - 1 <= kChunk, "draft positions of one step");
 
 // ------------------------------------------------------------- descriptors
-enum Prologue : int32_t { PRO_RMS_X = 0, PRO_GDN_OUT = 1, PRO_FA_OUT = 2, PRO_H = 3 };
+// PRO_MTP_IN: the MTP input rows [RMSNorm(h) w_h ; RMSNorm(emb) w_e], already
+// normalised by the MTP input phase.
+enum Prologue : int32_t { PRO_RMS_X = 0, PRO_GDN_OUT = 1, PRO_FA_OUT = 2, PRO_H = 3, PRO_MTP_IN = 4 };
 enum ZeroBuf : int32_t { ZERO_NONE = 0, ZERO_GU = 1, ZERO_YIN = 2 };
 // Outputs of one GEMM phase: input projections into yin, residual add into x
 // (then the 32-wide sums of squares for the next RMSNorm), gate/up pairs into
@@ -78,7 +83,7 @@ struct GemmDesc {
   int32_t n_tiles, nsb, n_out, pro, epi;
   int32_t img_in;    // 1: the activations come from the image the previous phase wrote
   int32_t img_out;   // 1: the epilogue writes the next phase's activation image
-  int32_t pad;
+  int32_t dump;      // EPI_TOP2: 1 = copy the logits to the debug buffer (main lm_head)
   const float* gain;      // RMSNorm gain (PRO_RMS_X) or per-head output-norm gain (PRO_GDN_OUT)
   const float* img_gain;  // gain the written image is multiplied by (NULL: none)
   // a buffer a later phase accumulates into, cleared (rows < R) at this phase's start
@@ -101,8 +106,19 @@ struct ModelDesc {
   int32_t max_seg;                    // partial slots per warp per phase
   int32_t grid;                       // blocks of the persistent launch
   float eps;
-  LayerDesc layer[MK_MAX_LAYERS];
+  // layer[n_layers] is the MTP block when has_mtp
+  LayerDesc layer[MK_MAX_LAYERS + 1];
   GemmDesc lm;
+  // MTP draft head: W_fc, and lm_head restricted to rows [0, draft_vocab)
+  int32_t has_mtp, n_draft, draft_vocab, pad_mtp;
+  GemmDesc mtp_fc, mtp_lm;
+  const float* mtp_norm_h;  // [H]
+  const float* mtp_norm_e;  // [H]
+  float* mtp_in;            // [kMaxRows][2H] normalised input rows of a draft pass
+  float* mtp_h;             // [kMaxSeqs][H] hidden output of the previous draft pass
+  float2* mtp_rope;         // [kMaxSeqs][kMaxDh/2] (cos, sin) at the next pass's position
+  int32_t* mtp_row;         // [kMaxSeqs][2] next pass's token and slot (position - cached length)
+  const double* inv_freq;   // [kMaxDh/2] rope_base^(-2i/dh)
   const float* final_norm;
   const uint8_t* embed;               // canonical [V][H/256] super-blocks
   // borrowed state
@@ -144,7 +160,8 @@ struct ModelDesc {
 constexpr int kOutTokens = 0;                  // [kMaxRows]
 constexpr int kOutCounts = kMaxRows;           // [kMaxSeqs]
 constexpr int kOutArgmax = kMaxRows + kMaxSeqs;  // [kMaxRows]
-constexpr int kOutInts = kOutArgmax + kMaxRows;
+constexpr int kOutDrafts = kOutArgmax + kMaxRows;  // [kMaxSeqs][kMaxDraft]
+constexpr int kOutInts = kOutDrafts + kMaxSeqs * kMaxDraft;
 
 struct StepDesc {
   int32_t R, n_seq, nt;               // rows, sequences, column tiles of 8

@@ -212,11 +212,40 @@ struct WarpCtx {
   uint32_t kv_pos;  // attention chunks consumed by this warp's group
 };
 
+// GEMM phases in step order: 4l + {0 input projections, 1 o_proj, 2 gate/up,
+// 3 down} for layer l, then 4 n_layers the lm_head, then per MTP draft pass p
+// six phases from mtp_gp0 + 6p: W_fc, input projections, o_proj, gate/up,
+// down, and the lm_head over the draft vocabulary.
+__device__ __forceinline__ int mtp_gp0(const ModelDesc& md) { return 4 * md.n_layers + 1; }
+
 __device__ __forceinline__ const GemmDesc& gemm_desc(const ModelDesc& md, int gp) {
   const int l = gp >> 2, part = gp & 3;
-  if (l >= md.n_layers) return md.lm;
-  const LayerDesc& L = md.layer[l];
-  return part == 0 ? L.in : part == 1 ? L.o : part == 2 ? L.gu : L.down;
+  if (l < md.n_layers) {
+    const LayerDesc& L = md.layer[l];
+    return part == 0 ? L.in : part == 1 ? L.o : part == 2 ? L.gu : L.down;
+  }
+  if (gp == 4 * md.n_layers) return md.lm;
+  const int q = (gp - mtp_gp0(md)) % 6;
+  const LayerDesc& M = md.layer[md.n_layers];
+  return q == 0 ? md.mtp_fc : q == 1 ? M.in : q == 2 ? M.o : q == 3 ? M.gu : q == 4 ? M.down : md.mtp_lm;
+}
+
+// Phases whose epilogue keeps top-1 records (the two lm_heads).
+__device__ __forceinline__ bool is_top_gp(const ModelDesc& md, int gp) {
+  return gp == 4 * md.n_layers || (gp > 4 * md.n_layers && (gp - mtp_gp0(md)) % 6 == 5);
+}
+
+// The attention whose KV pages are streamed right before GEMM phase gp (the
+// o_proj of a gated-attention layer or of an MTP pass), as a key that grows
+// along the step: layer l, or n_layers + p for draft pass p; -1 if none.
+__device__ __forceinline__ int attn_key_before(const ModelDesc& md, int gp) {
+  if (gp < 4 * md.n_layers) {
+    const int l = gp >> 2;
+    return ((gp & 3) == 1 && md.layer[l].kind == MK_LAYER_FA) ? l : -1;
+  }
+  if (gp <= 4 * md.n_layers) return -1;
+  const int q = gp - mtp_gp0(md);
+  return q % 6 == 2 ? md.n_layers + q / 6 : -1;
 }
 
 __device__ __forceinline__ Assign assign_for(const GemmDesc& g, int R, int grid, int cta, int warp) {
@@ -386,6 +415,8 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
         } else if (g.pro == PRO_FA_OUT) {
           s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
           s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.hq * md.dh + k));
+        } else if (g.pro == PRO_MTP_IN) {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.mtp_in + static_cast<size_t>(r) * 2 * md.H + k));
         } else {  // SwiGLU of the gate/up pair: 4 consecutive f share one 8-row block
           const float* gr = md.gu + static_cast<size_t>(r) * 2 * md.F + (k >> 3) * 16 + (k & 7);
           s1[b] = __ldcg(reinterpret_cast<const float4*>(gr));
@@ -434,6 +465,8 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
         } else if (g.pro == PRO_FA_OUT) {
           u[0] = s1[b].x * sigmoidf_(s2[b].x); u[1] = s1[b].y * sigmoidf_(s2[b].y);
           u[2] = s1[b].z * sigmoidf_(s2[b].z); u[3] = s1[b].w * sigmoidf_(s2[b].w);
+        } else if (g.pro == PRO_MTP_IN) {
+          u[0] = s1[b].x; u[1] = s1[b].y; u[2] = s1[b].z; u[3] = s1[b].w;
         } else {
           u[0] = siluf_(s1[b].x) * s2[b].x; u[1] = siluf_(s1[b].y) * s2[b].y;
           u[2] = siluf_(s1[b].z) * s2[b].z; u[3] = siluf_(s1[b].w) * s2[b].w;
@@ -515,11 +548,11 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
           if (r < R) {
             float x = -FLT_MAX;
             int ix = 0x7fffffff;
-            if (n < md.V) {
+            if (n < g.n_out) {
               x = v[r];
               ix = n;
               if (!isfinite(x)) atomicOr(&md.err[1], 1);
-              if (md.dbg_logits) md.dbg_logits[static_cast<size_t>(r) * md.V + n] = x;
+              if (md.dbg_logits && g.dump) md.dbg_logits[static_cast<size_t>(r) * md.V + n] = x;
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -824,7 +857,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
 
 __device__ __forceinline__ bool gemm_dispatch(const ModelDesc& md, const StepDesc& sd, int gp, const Smem& sm,
                                               WarpCtx& wc) {
-  const bool top = (gp >> 2) >= md.n_layers;
+  const bool top = is_top_gp(md, gp);
   switch (sd.nt) {
     case 1: return top ? gemm_phase<1, true>(md, sd, gp, sm, wc) : gemm_phase<1, false>(md, sd, gp, sm, wc);
     case 2: return top ? gemm_phase<2, true>(md, sd, gp, sm, wc) : gemm_phase<2, false>(md, sd, gp, sm, wc);
@@ -1447,6 +1480,27 @@ __device__ void attn_store_kv(const ModelDesc& md, int fa_i, int page, int kh, i
   }
 }
 
+// One row of K or V that an earlier phase of this launch stored into the pool
+// (an MTP draft pass reads back the positions of the catch-up rows and of the
+// passes before it), copied as stored into row t of the new-rows chunk.
+__device__ void attn_load_kv(const ModelDesc& md, int fa_i, int page, int kh, int slot, int which, uint8_t* tile,
+                             __half* tile_scales, const AttnSlot& SL, int t, int lane) {
+  const int dh = md.dh;
+  const size_t row = ((static_cast<size_t>(fa_i) * md.n_pages + page) * md.hkv + kh) * md.page_tokens + slot;
+  if (!md.kv_q8) {
+    const unsigned short* src = reinterpret_cast<const unsigned short*>(which ? md.kv_v : md.kv_k) + row * dh;
+    for (int d = lane; d < dh; d += 32)
+      *reinterpret_cast<unsigned short*>(tile + kv_off(SL, t, 2 * d)) = __ldcg(src + d);
+  } else {
+    const signed char* codes = reinterpret_cast<const signed char*>(which ? md.kv_v : md.kv_k) + row * dh;
+    const unsigned short* scales = (which ? md.kv_vs : md.kv_ks) + row * (dh / 32);
+    for (int d = lane; d < dh; d += 32)
+      tile[kv_off(SL, t, d)] = static_cast<uint8_t>(__ldcg(codes + d));
+    for (int b = lane; b < dh / 32; b += 32)
+      tile_scales[t * (dh / 32) + b] = __ushort_as_half(__ldcg(scales + b));
+  }
+}
+
 // Shared memory of the attention phase, inside the phase region.
 constexpr int kAttnQBytes = (kMaxQRows * (kMaxDh + 8) * 2 + 255) / 256 * 256;
 constexpr int kAttnNewBytes = 16384;                          // largest slot (fp16, dh 256)
@@ -1507,9 +1561,14 @@ __device__ __noinline__ void attn_combine(const ModelDesc& md, const StepDesc& s
   }
 }
 
+// mp > 0: MTP draft pass mp. Only the first row of each sequence is real: it
+// sits at slot k = mtp_row[si].slot (position = cached length + k) with RoPE
+// angles from mtp_rope; the new-rows chunk holds the slots 0..k-1 that earlier
+// phases of this launch stored (read back) and the row's own K/V at slot k,
+// all visible to it.
 template <bool Q8, bool SWZ>
 __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const Smem& sm,
-                                        float* scratch_row, WarpCtx& wc) {
+                                        float* scratch_row, WarpCtx& wc, int mp) {
   const LayerDesc& L = md.layer[layer];
   const int fa_i = L.fa_i;
   const int dh = md.dh, hkv = md.hkv, grp = md.hq / md.hkv;
@@ -1555,7 +1614,7 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
         for (int e = 0; e < 2; ++e) {
           const int dd = d + e, i = dd % (dh / 2);
           const float a = __ldcg(q + i), b = __ldcg(q + i + dh / 2);
-          const float2 cs = sd.rope[row][i];
+          const float2 cs = mp ? __ldcg(md.mtp_rope + si * (kMaxDh / 2) + i) : sd.rope[row][i];
           const float v = (dd < dh / 2 ? a * cs.x - b * cs.y : a * cs.y + b * cs.x) * q_scale;
           if (e == 0) v0 = v; else v1 = v;
         }
@@ -1563,21 +1622,31 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
       *reinterpret_cast<__half2*>(Qp + qr * qstride + pp) = __floats2half2_rn(v0, v1);
     }
     // the step's own rows (last split): RoPE k, store K/V into the pool, and
-    // keep the stored values as one more chunk, causal over the T rows
+    // keep the stored values as one more chunk, causal over the T rows (a
+    // draft pass: the earlier slots read back plus its own row, all visible)
+    const int k_own = mp ? min(max(__ldcg(md.mtp_row + 2 * si + 1), 0), kChunk - 1) : 0;
+    const int n_new = mp ? k_own + 1 : T;
     if (last) {
       for (int idx = tid; idx < SL.tx_bytes / 16; idx += kThreads)
         reinterpret_cast<uint4*>(newt)[idx] = make_uint4(0u, 0u, 0u, 0u);
       math_sync();
-      for (int t = warp; t < T; t += kWarps) {
-        const int row = row0 + t, pos = Lc + t;
+      for (int t = warp; t < n_new; t += kWarps) {
+        const int pos = Lc + t;
         const int page = pt[pos / md.page_tokens], slot = pos % md.page_tokens;
+        if (mp && t < k_own) {
+          attn_load_kv(md, fa_i, page, kh, slot, 0, newt, reinterpret_cast<__half*>(newt + SL.ks_off), SL, t, lane);
+          attn_load_kv(md, fa_i, page, kh, slot, 1, newt + SL.v_off, reinterpret_cast<__half*>(newt + SL.vs_off), SL,
+                       t, lane);
+          continue;
+        }
+        const int row = row0 + (mp ? 0 : t);
         const float* kr = md.yin + static_cast<size_t>(row) * md.n_in_max + kq_off + kh * dh;
         const float* vr = md.yin + static_cast<size_t>(row) * md.n_in_max + vq_off + kh * dh;
         float* ksr = scratch_row + warp * 2 * kMaxDh;  // per-warp staging in global scratch
         float* vsr = ksr + kMaxDh;
         for (int i = lane; i < dh / 2; i += 32) {
           const float a = __ldcg(kr + i), b = __ldcg(kr + i + dh / 2);
-          const float2 cs = sd.rope[row][i];
+          const float2 cs = mp ? __ldcg(md.mtp_rope + si * (kMaxDh / 2) + i) : sd.rope[row][i];
           ksr[i] = a * cs.x - b * cs.y;
           ksr[i + dh / 2] = a * cs.y + b * cs.x;
         }
@@ -1608,7 +1677,7 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
         const bool cached = i < it.nch;
         const int slot = tg * spg + static_cast<int>(wc.kv_pos % static_cast<uint32_t>(spg));
         const uint8_t* cb = newt;
-        int nvalid = T, causal = grp;
+        int nvalid = n_new, causal = mp ? 0 : grp;
         if (cached) {
           if (ok)
             ok = mbar_wait_bounded(ab.full + slot, (wc.kv_pos / spg) & 1u, md, sd.barrier_timeout_ns,
@@ -1725,10 +1794,11 @@ static_assert(kWarps * (2 * kMaxT * 128 + kMaxT * 10) * 4 <= kPhaseBytes, "Gated
 // When lm_head's reduction is sliced, every tile is split and its logits were
 // summed in md.logits; after the barrier each warp scans tiles gid, gid +
 // (warps), ... and merges them into its top-1 record (ties: lowest index).
-__device__ __noinline__ void lm_argmax(const ModelDesc& md, const StepDesc& sd, const WarpCtx& wc) {
+__device__ __noinline__ void lm_argmax(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g,
+                                      const WarpCtx& wc) {
   const int R = sd.R, lane = wc.lane;
   const int nw = gridDim.x * kWarps;
-  const int ntile = (md.V + kTileRows - 1) / kTileRows;
+  const int ntile = g.n_tiles;
   float b[kMaxRows];
   int bi[kMaxRows];
 #pragma unroll
@@ -1738,13 +1808,13 @@ __device__ __noinline__ void lm_argmax(const ModelDesc& md, const StepDesc& sd, 
   }
   for (int t = wc.gid; t < ntile; t += nw) {
     const int n = t * kTileRows + lane;
-    if (n < md.V) {
+    if (n < g.n_out) {
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r)
         if (r < R) {
           const float x = __ldcg(md.logits + static_cast<size_t>(r) * md.V + n);
           if (!isfinite(x)) atomicOr(&md.err[1], 1);
-          if (md.dbg_logits) md.dbg_logits[static_cast<size_t>(r) * md.V + n] = x;
+          if (md.dbg_logits && g.dump) md.dbg_logits[static_cast<size_t>(r) * md.V + n] = x;
           top1_merge(b[r], bi[r], x, n);
         }
     }
@@ -1814,6 +1884,119 @@ __device__ void verify_phase(const ModelDesc& md, const StepDesc& sd, const Smem
   }
 }
 
+// ------------------------------------------------------- MTP draft head
+// One element of the embedding matrix (Q4 super-blocks, row `tok`).
+__device__ __forceinline__ float embed_value(const ModelDesc& md, int tok, int k) {
+  const int nsbH = md.H / 256, sb = k >> 8, j = (k & 255) >> 5, i = k & 31;
+  const uint8_t* blk = md.embed + (static_cast<size_t>(tok) * nsbH + sb) * 144;
+  const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(blk));
+  const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+  const uint64_t lo64 = hdr.y | (static_cast<uint64_t>(hdr.z) << 32);
+  const uint64_t mid64 = hdr.z | (static_cast<uint64_t>(hdr.w) << 32);
+  const float sc = static_cast<float>((lo64 >> (6 * j)) & 63u);
+  const float m = static_cast<float>((mid64 >> (16 + 6 * j)) & 63u);
+  const uint8_t byte = __ldg(blk + 16 + 16 * j + (i % 16));
+  const int q = i < 16 ? (byte & 15) : (byte >> 4);
+  return (d * sc) * static_cast<float>(q) - dmin * m;
+}
+
+// Input rows of MTP draft pass p, one block per step row r:
+//   mtp_in[r] = [RMSNorm(h) w_h ; RMSNorm(embed(tok)) w_e]
+// with (h, tok) = (final hidden state of row r, its greedy token) in pass 0 and
+// (the previous pass's hidden output, its draft) for the first row of each
+// sequence in later passes (the other rows are zero). Also clears x[r], which
+// W_fc's epilogue adds into, and the draft-logit rows the sliced lm_head sums into.
+__device__ __noinline__ void mtp_input_phase(const ModelDesc& md, const StepDesc& sd, int p, const Smem& sm) {
+  const int H = md.H, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const int stride = gridDim.x * kThreads, t0 = blockIdx.x * kThreads + tid;
+    for (int idx = t0; idx < sd.R * md.draft_vocab; idx += stride)
+      md.logits[static_cast<size_t>(idx / md.draft_vocab) * md.V + idx % md.draft_vocab] = 0.f;
+  }
+  float* red = sm.misc() + 512;  // [warp][2] partial sums of squares
+  for (int r = blockIdx.x; r < sd.R; r += gridDim.x) {
+    const int si = sd.row_si[r];
+    const bool real = p == 0 || r == sd.seq_row0[si];
+    const float* h = p == 0 ? md.x + static_cast<size_t>(r) * H : md.mtp_h + static_cast<size_t>(si) * H;
+    // (an all-NaN row leaves no argmax: the non-finite flag reports it; keep the index in range)
+    const int tok = !real ? 0 : min(max(p == 0 ? __ldcg(md.out + kOutArgmax + r) : __ldcg(md.mtp_row + 2 * si), 0),
+                                    md.V - 1);
+    float* dst = md.mtp_in + static_cast<size_t>(r) * 2 * H;
+    float sh = 0.f, se = 0.f;
+    for (int k = tid; k < H; k += kThreads) {
+      const float hv = real ? __ldcg(h + k) : 0.f;
+      const float ev = real ? embed_value(md, tok, k) : 0.f;
+      sh = fmaf(hv, hv, sh);
+      se = fmaf(ev, ev, se);
+      dst[k] = hv;
+      dst[H + k] = ev;
+    }
+    sh = warp_sum(sh);
+    se = warp_sum(se);
+    if (lane == 0) {
+      red[2 * warp] = sh;
+      red[2 * warp + 1] = se;
+    }
+    math_sync();
+    float th = 0.f, te = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      th += red[2 * w];
+      te += red[2 * w + 1];
+    }
+    const float rh = 1.0f / sqrtf(th / static_cast<float>(H) + md.eps);
+    const float re = 1.0f / sqrtf(te / static_cast<float>(H) + md.eps);
+    for (int k = tid; k < H; k += kThreads) {
+      dst[k] = dst[k] * rh * md.mtp_norm_h[k];
+      dst[H + k] = dst[H + k] * re * md.mtp_norm_e[k];
+      md.x[static_cast<size_t>(r) * H + k] = 0.f;
+    }
+    math_sync();  // red is reused by the next row
+  }
+}
+
+// Block 0: draft p of every sequence = argmax over the draft vocabulary of
+// its source row (pass 0: the last accepted row a; later passes: the first
+// row), lowest index on ties. Unless p is the last pass, it also prepares
+// pass p+1: the token (this draft), the slot a + p + 1, its RoPE angles in
+// double precision, and the hidden state (the source row's x).
+__device__ __noinline__ void draft_phase(const ModelDesc& md, const StepDesc& sd, int p) {
+  if (blockIdx.x != 0) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nrec = gridDim.x * kWarps;
+  for (int si = warp; si < sd.n_seq; si += kWarps) {
+    const int a = __ldcg(md.out + kOutCounts + si) - 1;
+    const int rs = p == 0 ? sd.seq_row0[si] + a : sd.seq_row0[si];
+    float b1 = -FLT_MAX;
+    int i1 = 0x7fffffff;
+    for (int gidx = lane; gidx < nrec; gidx += 32)
+      top1_merge(b1, i1, __ldcg(md.top_val + static_cast<size_t>(gidx) * kMaxRows + rs),
+                 __ldcg(md.top_idx + static_cast<size_t>(gidx) * kMaxRows + rs));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob1 = __shfl_xor_sync(0xffffffffu, b1, o);
+      const int oi1 = __shfl_xor_sync(0xffffffffu, i1, o);
+      top1_merge(b1, i1, ob1, oi1);
+    }
+    if (lane == 0) md.out[kOutDrafts + si * kMaxDraft + p] = i1;
+    if (p + 1 < md.n_draft) {
+      const int k = a + p + 1;
+      if (lane == 0) {
+        md.mtp_row[2 * si] = i1;
+        md.mtp_row[2 * si + 1] = k;
+      }
+      const double pos = static_cast<double>(sd.seq_len[si] + k);
+      for (int i = lane; i < md.dh / 2; i += 32) {
+        double sn, cs;
+        sincos(pos * md.inv_freq[i], &sn, &cs);
+        md.mtp_rope[si * (kMaxDh / 2) + i] = make_float2(static_cast<float>(cs), static_cast<float>(sn));
+      }
+      for (int k2 = lane; k2 < md.H; k2 += 32)
+        md.mtp_h[static_cast<size_t>(si) * md.H + k2] = __ldcg(md.x + static_cast<size_t>(rs) * md.H + k2);
+    }
+  }
+}
+
 // ------------------------------------------------------------ the producer
 // Lanes 0..kWarps-1 each walk one math warp's unit sequence; the warp stays
 // converged: every sweep, each lane issues its next unit if that unit's slot
@@ -1821,7 +2004,7 @@ __device__ void verify_phase(const ModelDesc& md, const StepDesc& sd, const Smem
 // the o_proj units of an attention layer the whole warp stops: once every
 // ring is drained it streams that layer's KV pages through the same shared
 // memory (attn_stream), then resumes the weights.
-__device__ void producer_warp(const ModelDesc& md, const StepDesc& sd, const Smem& sm, const CUtensorMap* tmk,
+__device__ __noinline__ void producer_warp(const ModelDesc& md, const StepDesc& sd, const Smem& sm, const CUtensorMap* tmk,
                               const CUtensorMap* tmv) {
   const int lane = threadIdx.x & 31;
   const int w = lane < kWarps ? lane : 0;
@@ -1836,14 +2019,15 @@ __device__ void producer_warp(const ModelDesc& md, const StepDesc& sd, const Sme
   bool failed = false;
   volatile int32_t* err = md.err;
   uint64_t t_idle = 0;
+  const int last_gp = md.has_mtp ? mtp_gp0(md) + 6 * md.n_draft - 1 : 4 * md.n_layers;
   for (uint32_t sweep = 0;; ++sweep) {
     // advance to the next phase with units for this lane's warp
     while (!done && left == 0 && hold < 0) {
       const int ngp = gp + 1;
-      if (ngp > 4 * md.n_layers) { done = true; break; }
-      const int l = ngp >> 2;
-      if ((ngp & 3) == 1 && l < md.n_layers && md.layer[l].kind == MK_LAYER_FA && l > attn_done_upto) {
-        hold = l;
+      if (ngp > last_gp) { done = true; break; }
+      const int ak = attn_key_before(md, ngp);
+      if (ak >= 0 && ak > attn_done_upto) {
+        hold = ak;
         break;
       }
       gp = ngp;
@@ -1866,7 +2050,7 @@ __device__ void producer_warp(const ModelDesc& md, const StepDesc& sd, const Sme
         ok = mbar_wait_bounded(sm.empty(w, (p - 1) % kRing), ((p - 1) / kRing) & 1u, md, sd.barrier_timeout_ns,
                                DEV_COPY_TIMEOUT);
       ok = __all_sync(0xffffffffu, ok);
-      if (ok) ok = attn_stream(md, sd, sm, hl, tmk, tmv, kv_issued, pol);
+      if (ok) ok = attn_stream(md, sd, sm, hl < md.n_layers ? hl : md.n_layers, tmk, tmv, kv_issued, pol);
       if (!ok) { failed = true; break; }
       attn_done_upto = hl;
       if (lane < kWarps) hold = -1;
@@ -1944,39 +2128,59 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
   int nbar = 0;
   float* my_scratch = attn_scratch + static_cast<size_t>(blockIdx.x) * kWarps * 2 * kMaxDh;
   // Phases: 0 embed; then per layer l: 1+5l input GEMM, 2+5l mixer,
-  // 3+5l o_proj, 4+5l gate/up, 5+5l down; then lm_head; then verify.
-  const int n_phases = 1 + 5 * md.n_layers + 2;
+  // 3+5l o_proj, 4+5l gate/up, 5+5l down; then lm_head; then verify. With an
+  // MTP head, nine more per draft pass p: input rows, W_fc, input
+  // projections, attention, o_proj, gate/up, down, draft lm_head, draft.
+  const int n_main = 1 + 5 * md.n_layers + 2;
+  const int n_phases = n_main + (md.has_mtp ? 9 * md.n_draft : 0);
+  auto attention = [&](int layer, int mp) {
+    if (!md.kv_q8) return attn_phase<false, true>(md, sd, layer, sm, my_scratch, wc, mp);
+    if (md.dh % 128 == 0) return attn_phase<true, true>(md, sd, layer, sm, my_scratch, wc, mp);
+    return attn_phase<true, false>(md, sd, layer, sm, my_scratch, wc, mp);
+  };
   if (md.dbg_time && blockIdx.x == 0 && threadIdx.x == 0) md.dbg_time[0] = globaltimer();
   for (int ph = 0; ph < n_phases; ++ph) {
     bool ok = true;
     int gp = -1;
     if (ph == 0) {
       embed_phase(md, sd, wc);
-    } else if (ph == n_phases - 1) {
+    } else if (ph == n_main - 1) {
       verify_phase(md, sd, sm);
-      break;
-    } else if (ph == n_phases - 2) {
+      if (!md.has_mtp) break;
+    } else if (ph == n_main - 2) {
       gp = 4 * md.n_layers;
-    } else {
+    } else if (ph < n_main) {
       const int l = (ph - 1) / 5, part = (ph - 1) % 5;
       if (part == 1) {
         if (md.layer[l].kind == MK_LAYER_GDN) gdn_phase(md, sd, l, wc, sm);
-        else if (!md.kv_q8) ok = attn_phase<false, true>(md, sd, l, sm, my_scratch, wc);
-        else if (md.dh % 128 == 0) ok = attn_phase<true, true>(md, sd, l, sm, my_scratch, wc);
-        else ok = attn_phase<true, false>(md, sd, l, sm, my_scratch, wc);
+        else ok = attention(l, 0);
       } else {
         gp = 4 * l + (part == 0 ? 0 : part - 1);
+      }
+    } else {
+      const int q = ph - n_main, mp = q / 9, part = q % 9;
+      const int g0 = mtp_gp0(md) + 6 * mp;
+      if (part == 0) mtp_input_phase(md, sd, mp, sm);
+      else if (part <= 2) gp = g0 + part - 1;
+      else if (part == 3) ok = attention(md.n_layers, mp);
+      else if (part <= 7) gp = g0 + part - 2;
+      else {
+        draft_phase(md, sd, mp);
+        if (mp + 1 == md.n_draft) break;  // nothing in the launch reads the last drafts
       }
     }
     if (gp >= 0) ok = gemm_dispatch(md, sd, gp, sm, wc);
     // a failed wait inside a phase still meets the barrier, which reports it
     bool synced = grid_sync(md, sd, nbar, &sflag);
-    if (md.dbg_time && blockIdx.x == 0 && threadIdx.x == 0) md.dbg_time[ph + 1] = globaltimer();
+    if (md.dbg_time && ph < n_main && blockIdx.x == 0 && threadIdx.x == 0) md.dbg_time[ph + 1] = globaltimer();
     if (!synced || !ok) break;
-    if (ph == n_phases - 2 && make_sched(md.lm.nsb, sd.R).S > 1) {  // sliced lm_head: scan the summed logits
-      lm_argmax(md, sd, wc);
-      synced = grid_sync(md, sd, nbar, &sflag);
-      if (!synced) break;
+    if (gp >= 0 && is_top_gp(md, gp)) {
+      const GemmDesc& g = gemm_desc(md, gp);
+      if (make_sched(g.nsb, sd.R).S > 1) {  // sliced lm_head: scan the summed logits
+        lm_argmax(md, sd, g, wc);
+        synced = grid_sync(md, sd, nbar, &sflag);
+        if (!synced) break;
+      }
     }
   }
 }

@@ -43,6 +43,7 @@ class mk_layout(ctypes.Structure):
         ("tied_lm_head", i32), ("has_mtp", i32), ("draft_vocab", i32),
         ("kv_dtype", i32), ("page_tokens", i32), ("n_pages", i32), ("max_seqs", i32),
         ("max_pages_per_seq", i32), ("n_state_slots", i32), ("rms_eps", f32),
+        ("n_draft", i32),
     ]
 
 
@@ -56,7 +57,9 @@ class mk_layer_weights(ctypes.Structure):
 
 class mk_weights(ctypes.Structure):
     _fields_ = [("embed", vp), ("final_norm", vp), ("lm_head", vp),
-                ("layers", mk_layer_weights * MK_MAX_LAYERS)]
+                ("layers", mk_layer_weights * MK_MAX_LAYERS),
+                ("mtp", mk_layer_weights), ("mtp_fc", vp), ("mtp_norm_h", vp), ("mtp_norm_e", vp),
+                ("mtp_final_norm", vp)]
 
 
 class mk_buffers(ctypes.Structure):
@@ -84,6 +87,7 @@ def _load():
         "mk_step_prepare": (i32, [vp, i32, vp, vp, vp, vp]),
         "mk_step_launch": (i32, [vp]),
         "mk_step_finish": (i32, [vp, vp, vp]),
+        "mk_last_drafts": (i32, [vp, vp]),
         "mk_commit": (i32, [vp, i32, vp, vp]),
         "mk_debug_outputs": (i32, [vp, vp, vp]),
         "mk_last_launch_ms": (f32, [vp]),
@@ -108,7 +112,7 @@ lib = _load()
 
 EXPORTS = ["mk_packed_bytes", "mk_kv_bytes", "mk_kv_scale_bytes", "mk_gdn_state_bytes",
            "mk_conv_state_bytes", "mk_create", "mk_free", "mk_seq_set", "mk_seq_reset", "mk_seq_get",
-           "mk_step", "mk_step_prepare", "mk_step_launch", "mk_step_finish", "mk_commit",
+           "mk_step", "mk_step_prepare", "mk_step_launch", "mk_step_finish", "mk_last_drafts", "mk_commit",
            "mk_debug_outputs", "mk_last_launch_ms", "mk_debug_skip_arrival", "mk_grid_blocks",
            "mk_status_str", "mk_debug_scratch", "mk_step_io_bytes", "mk_step_static",
            "mk_debug_timeline", "mk_debug_gemm_schedule", "mk_debug_act_bytes"]
@@ -139,8 +143,10 @@ def _check(rc: int, what: str):
 
 
 def make_layout(model: dict, kv_q8: int, n_pages: int, max_seqs: int = MK_MAX_SEQS,
-                max_pages_per_seq: int | None = None, n_state_slots: int = MK_MAX_T + 1) -> mk_layout:
-    """mk_layout from a model description dict (keys as in gen/configs.py)."""
+                max_pages_per_seq: int | None = None, n_state_slots: int = MK_MAX_T + 1,
+                n_draft: int = 0) -> mk_layout:
+    """mk_layout from a model description dict (keys as in gen/configs.py);
+    n_draft: drafts per step of the MTP head (models with has_mtp)."""
     L = mk_layout()
     L.n_layers, L.hidden, L.ffn, L.vocab = model["n_layers"], model["hidden"], model["ffn"], model["vocab"]
     for i, k in enumerate(model["kinds"]):
@@ -149,8 +155,9 @@ def make_layout(model: dict, kv_q8: int, n_pages: int, max_seqs: int = MK_MAX_SE
     L.gdn_hk, L.gdn_hv, L.gdn_dk, L.gdn_dv, L.conv_w = (model["hk"], model["hv"], model["dk"], model["dv"],
                                                          model["conv_w"])
     L.tied_lm_head = model["tied"]
-    L.has_mtp = 0
-    L.draft_vocab = 0
+    L.has_mtp = int(model.get("has_mtp", 0))
+    L.draft_vocab = int(model.get("draft_vocab", 0)) if L.has_mtp else 0
+    L.n_draft = int(n_draft) if L.has_mtp else 0
     L.kv_dtype = MK_KV_Q8 if kv_q8 else MK_KV_F16
     L.page_tokens = 16
     L.n_pages = n_pages
@@ -169,12 +176,12 @@ class Engine:
 
     def __init__(self, model: dict, weights: dict, kv_q8: int, n_pages: int, max_seqs: int = MK_MAX_SEQS,
                  device: str = "cuda:0", stream=None, max_pages_per_seq: int | None = None,
-                 n_state_slots: int = MK_MAX_T + 1):
+                 n_state_slots: int = MK_MAX_T + 1, n_draft: int = 0):
         import torch
         self.torch = torch
         self.model = model
         self.device = torch.device(device)
-        self.layout = make_layout(model, kv_q8, n_pages, max_seqs, max_pages_per_seq, n_state_slots)
+        self.layout = make_layout(model, kv_q8, n_pages, max_seqs, max_pages_per_seq, n_state_slots, n_draft)
         Lp = ctypes.byref(self.layout)
         nbytes = lib.mk_packed_bytes(Lp)
         if nbytes == 0:
@@ -202,6 +209,15 @@ class Engine:
                 key = f"layers.{li}.{n}"
                 if key in dev:
                     setattr(W.layers[li], n, dev[key].data_ptr())
+        if self.layout.has_mtp:
+            for n in LAYER_FIELDS:
+                key = f"mtp.block.{n}"
+                if key in dev:
+                    setattr(W.mtp, n, dev[key].data_ptr())
+            W.mtp_fc = dev["mtp.fc"].data_ptr()
+            W.mtp_norm_h = dev["mtp.norm_h"].data_ptr()
+            W.mtp_norm_e = dev["mtp.norm_e"].data_ptr()
+            W.mtp_final_norm = dev["mtp.final_norm"].data_ptr()
         B = mk_buffers()
         B.packed = self.packed.data_ptr()
         B.kv_k, B.kv_v = self.kv_k.data_ptr(), self.kv_v.data_ptr()
@@ -231,8 +247,8 @@ class Engine:
 
     def kv_views(self):
         m, torch = self.model, self.torch
-        n_fa = sum(1 for k in m["kinds"] if k == 1)
-        shape = (n_fa, self.layout.n_pages, m["hkv"], 16, m["dh"])
+        n_kv = sum(1 for k in m["kinds"] if k == 1) + (1 if self.layout.has_mtp else 0)
+        shape = (n_kv, self.layout.n_pages, m["hkv"], 16, m["dh"])
         n = int(np.prod(shape))
         if self.layout.kv_dtype == MK_KV_Q8:
             sshape = shape[:-1] + (m["dh"] // 32,)
@@ -319,6 +335,12 @@ class Engine:
         out_c = np.zeros(self._nseq, np.int32)
         _check(lib.mk_step_finish(self.ctx, _np_ptr(out_t), _np_ptr(out_c)), "mk_step_finish")
         return out_t[: int(out_c.sum())], out_c
+
+    def last_drafts(self, n_seq: int):
+        """MTP drafts of the last completed step: [n_seq][n_draft]."""
+        d = np.zeros((n_seq, max(1, self.layout.n_draft)), np.int32)
+        _check(lib.mk_last_drafts(self.ctx, _np_ptr(d)), "mk_last_drafts")
+        return d
 
     def commit(self, seq_ids, n_keep):
         s = np.ascontiguousarray(seq_ids, np.int32)

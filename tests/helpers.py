@@ -38,10 +38,12 @@ class Pair:
         self.torch = torch
         self.wl = Workload(name, norm_jitter=norm_jitter, overrides=overrides, nthreads=nthreads, **kw)
         wl = self.wl
+        self.n_draft = int(wl.spec.get("n_draft", 0)) if wl.model.get("has_mtp") else 0
         self.orc_pool = copy.deepcopy(wl.pool)
         self.oracle = orc.Oracle(wl.model, wl.weights, self.orc_pool, wl.kv_q8, wl.n_pages, wl.max_seqs,
-                                 nthreads=nthreads)
-        self.eng = mk.Engine(wl.model, wl.weights, wl.kv_q8, wl.n_pages, max_seqs=wl.max_seqs)
+                                 nthreads=nthreads, n_draft=self.n_draft)
+        self.eng = mk.Engine(wl.model, wl.weights, wl.kv_q8, wl.n_pages, max_seqs=wl.max_seqs,
+                             n_draft=self.n_draft)
         self.eng.load_pool(wl.pool)
         for s, (cached, _T) in enumerate(wl.seqs):
             S, conv = wl.states[s]
@@ -109,7 +111,29 @@ class Pair:
         assert ec <= REL_L2_TOL, f"seq {seq}: conv state rel L2 {ec}"
         return dict(state_rel_l2=es, conv_rel_l2=ec)
 
-    def compare_kv(self, seq, positions):
+    def compare_drafts(self, seq_order, counts_match):
+        """MTP drafts of the last step, per sequence in step order: equal to the
+        oracle's up to the first draft whose oracle top-2 gap is below
+        TIE_GAP * rms (the chain may legitimately diverge from there; the rest
+        is counted as excused). Sequences whose accepted counts differ (an
+        excused near-tie in verify) are skipped. Returns (compared, excused)."""
+        gd = self.eng.last_drafts(len(seq_order))
+        compared = excused = 0
+        for i, s in enumerate(seq_order):
+            if not counts_match[i]:
+                excused += self.n_draft
+                continue
+            od = self.oracle.drafts(s)
+            for j in range(self.n_draft):
+                if od["gap"][j] < TIE_GAP * od["rms"][j]:
+                    excused += self.n_draft - j
+                    break
+                assert int(gd[i][j]) == int(od["tokens"][j]), \
+                    f"seq {s} draft {j}: gpu {gd[i].tolist()} oracle {od['tokens'].tolist()}"
+                compared += 1
+        return compared, excused
+
+    def compare_kv(self, seq, positions, layers=None):
         """New positions of one sequence in every attention layer.
 
         fp16 pool: every stored head vector within relative L2 1e-3 of the
@@ -124,6 +148,8 @@ class Pair:
         for name, v in views.items():
             g = v.cpu().numpy()
             o = self.orc_pool[name].view(g.dtype)
+            if layers is not None:
+                g, o = g[list(layers)], o[list(layers)]
             for p in positions:
                 page, slot = table[p // 16], p % 16
                 gg, oo = g[:, page, :, slot], o[:, page, :, slot]

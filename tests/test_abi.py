@@ -78,3 +78,23 @@ def test_layout_rejections(mk):
 def test_status_strings(mk):
     for code in mk.STATUS:
         assert mk.lib.mk_status_str(code)
+
+
+def test_mtp_layout_sizes_and_rejections(mk):
+    """With an MTP head the pool gains one KV layer and the packed buffer the
+    head's matrices (W_fc 2H->H and one gated-attention layer); n_draft and
+    draft_vocab are range-checked."""
+    m = dict(configs.QWEN27, has_mtp=1, draft_vocab=32768)
+    base = mk.make_layout(configs.QWEN27, kv_q8=0, n_pages=320, max_seqs=1)
+    L = mk.make_layout(m, kv_q8=0, n_pages=320, max_seqs=1, n_draft=4)
+    d = configs.model_dims(m)
+    assert mk.lib.mk_kv_bytes(ctypes.byref(L)) == (d["n_fa"] + 1) * 320 * m["hkv"] * 16 * m["dh"] * 2
+    H, F = m["hidden"], m["ffn"]
+    head = (H * 2 * H + (2 * d["fa_q"] + 2 * d["fa_kv"]) * H + H * d["fa_q"] + 3 * F * H) * 0.5625
+    extra = mk.lib.mk_packed_bytes(ctypes.byref(L)) - mk.lib.mk_packed_bytes(ctypes.byref(base))
+    assert head <= extra <= head * 1.01
+    for kw in (dict(n_draft=0), dict(n_draft=mk.MK_MAX_T)):
+        bad = mk.make_layout(m, kv_q8=0, n_pages=320, max_seqs=1, **kw)
+        assert mk.lib.mk_packed_bytes(ctypes.byref(bad)) == 0, kw
+    bad = mk.make_layout(dict(m, draft_vocab=m["vocab"] + 1), kv_q8=0, n_pages=320, max_seqs=1, n_draft=4)
+    assert mk.lib.mk_packed_bytes(ctypes.byref(bad)) == 0

@@ -13,13 +13,15 @@ import pytest
 
 pytestmark = pytest.mark.gpu
 
-from helpers import Pair  # noqa: E402
+from helpers import Pair, configs  # noqa: E402
 
 CASES = {
     # name: (workload, overrides)
     "t1-4k-fp16": ("qwen27-t1-4k-fp16", None),
     "t5-4k-fp16": ("qwen27-t1-4k-fp16", dict(seqs=[(4096, 5)])),
     "4x3-23k-q8": ("qwen27-4x3-23k-q8", None),
+    # T = 5 with the MTP draft head: four drafts per step over the first 32,768 tokens
+    "t5-4k-fp16-mtp": ("qwen27-t5-4k-fp16-mtp", None),
 }
 
 
@@ -36,9 +38,16 @@ def test_qwen27_full_step(cuda_ok, case):
     co = [int(c) for c in ro["counts"]]
     cg = [int(c) for c in rg["counts"]]
     seqs = list(range(len(wl.seqs)))
+    n_fa = configs.model_dims(wl.model)["n_fa"]
+    if p.n_draft:
+        print(case, "drafts compared/excused", p.compare_drafts(seqs, [a == b for a, b in zip(co, cg)]))
+        for s in seqs:
+            if co[s] == cg[s]:
+                r0 = wl.seqs[s][0]
+                p.compare_kv(s, list(range(r0, r0 + co[s] + p.n_draft - 1)), layers=[n_fa])
     p.oracle.commit(seqs, co)
     p.eng.commit(seqs, cg)
     for s in seqs:
-        p.compare_kv(s, [int(x) for x, q in zip(pos, sid) if q == s])
+        p.compare_kv(s, [int(x) for x, q in zip(pos, sid) if q == s], layers=range(n_fa))
         if co[s] == cg[s]:  # a near-tie may legitimately change the accepted length
             p.compare_state(s)
