@@ -279,8 +279,11 @@ def run_ours(args, world, rank, local):
     ms = total_ms / args.steps
 
     # ---- end to end through mk_step (host rows in, accepted tokens out)
+    def drafts():
+        return eng.last_drafts(len(wl.seqs)) if n_draft else None
+
     for _ in range(2):
-        out_t, out_c = eng.step(*next_rows(wl, tok, pos, sid, out_t, out_c, rng))
+        out_t, out_c = eng.step(*next_rows(wl, tok, pos, sid, out_t, out_c, rng, drafts()))
         tok, pos, sid = last_rows
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -288,7 +291,7 @@ def run_ours(args, world, rank, local):
     accepted = 0
     h2d = d2h = 0
     for _ in range(args.e2e_steps):
-        rows = next_rows(wl, tok, pos, sid, out_t, out_c, rng)
+        rows = next_rows(wl, tok, pos, sid, out_t, out_c, rng, drafts())
         out_t, out_c = eng.step(*rows)
         tok, pos, sid = last_rows
         accepted += int(out_c.sum())
@@ -311,6 +314,8 @@ def run_ours(args, world, rank, local):
             "config": {"workload": args.workload if not args.layers else f"{args.workload} (first {args.layers} layers: profiling stand-in)",
                        "rows_per_step": R, "sequences": len(wl.seqs),
                        "cached_tokens": [c for c, _T in wl.seqs], "kv": "q8" if wl.kv_q8 else "fp16",
+                       "mtp": ({"n_draft": n_draft, "draft_vocab": wl.model["draft_vocab"],
+                                "drafts": "next step's drafts are the head's (e2e loop)"} if n_draft else None),
                        "l2": "inputs larger than L2: 14.4 GB of weights streamed per step",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "step_us": ms * 1e3,
@@ -335,9 +340,10 @@ def run_ours(args, world, rank, local):
 last_rows = None
 
 
-def next_rows(wl, tok, pos, sid, out_t, out_c, rng):
+def next_rows(wl, tok, pos, sid, out_t, out_c, rng, drafts=None):
     """Next verify step of a greedy decode loop: each sequence's first row is
-    its bonus token at the new length, the other rows random drafts."""
+    its bonus token at the new length, the other rows the MTP head's drafts of
+    the step before (drafts [sequence][n_draft]) or random tokens."""
     global last_rows
     new_tok, new_pos, new_sid = [], [], []
     at = 0
@@ -346,7 +352,9 @@ def next_rows(wl, tok, pos, sid, out_t, out_c, rng):
         bonus = int(out_t[at + c - 1])
         at += c
         base = int(np.asarray(pos)[np.asarray(sid) == i][0]) + c
-        new_tok += [bonus] + [int(x) for x in rng.integers(0, wl.model["vocab"], T - 1)]
+        d = [] if drafts is None else [int(x) for x in drafts[i][: T - 1]]
+        d += [int(x) for x in rng.integers(0, wl.model["vocab"], T - 1 - len(d))]
+        new_tok += [bonus] + d
         new_pos += list(range(base, base + T))
         new_sid += [i] * T
     last_rows = (np.array(new_tok, np.int32), np.array(new_pos, np.int32), np.array(new_sid, np.int32))

@@ -570,7 +570,6 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
       (e = dev_alloc(c, &md.img_p[0], static_cast<size_t>(md.img_k / 16) * kMaxRows * 4)) ||
       (e = dev_alloc(c, &md.img_p[1], static_cast<size_t>(md.img_k / 16) * kMaxRows * 4)) ||
       (e = dev_alloc(c, &md.x, static_cast<size_t>(kMaxRows) * H * 4)) ||
-      (e = dev_alloc(c, &md.xsq, static_cast<size_t>(H / 32) * kMaxRows * 4)) ||
       (e = dev_alloc(c, &md.yin, static_cast<size_t>(kMaxRows) * p.n_in_max * 4)) ||
       (e = dev_alloc(c, &md.o, static_cast<size_t>(kMaxRows) * std::max(1, p.o_stride) * 4)) ||
       (e = dev_alloc(c, &md.h, static_cast<size_t>(kMaxRows) * F * 4)) ||
@@ -976,7 +975,7 @@ constexpr int kMaxDevices = 64;
 void* g_static_addr[kMaxDevices] = {nullptr};
 
 struct StaticLayout {
-  size_t md, img_h0, img_h1, img_p0, img_p1, x, xsq, yin, o, h, gu, logits, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
+  size_t md, img_h0, img_h1, img_p0, img_p1, x, yin, o, h, gu, logits, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
       attn_scratch, total;
 };
 
@@ -992,7 +991,6 @@ StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
   take(L.img_p0, static_cast<size_t>(md.img_k / 16) * kMaxRows * 4);
   take(L.img_p1, static_cast<size_t>(md.img_k / 16) * kMaxRows * 4);
   take(L.x, static_cast<size_t>(kMaxRows) * md.H * 4);
-  take(L.xsq, static_cast<size_t>(md.H / 32) * kMaxRows * 4);
   take(L.yin, static_cast<size_t>(kMaxRows) * md.n_in_max * 4);
   take(L.o, static_cast<size_t>(kMaxRows) * std::max(1, md.o_stride) * 4);
   take(L.h, static_cast<size_t>(kMaxRows) * md.F * 4);
@@ -1040,7 +1038,6 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
   md.img_p[0] = reinterpret_cast<float*>(base + SL.img_p0);
   md.img_p[1] = reinterpret_cast<float*>(base + SL.img_p1);
   md.x = reinterpret_cast<float*>(base + SL.x);
-  md.xsq = reinterpret_cast<float*>(base + SL.xsq);
   md.yin = reinterpret_cast<float*>(base + SL.yin);
   md.o = reinterpret_cast<float*>(base + SL.o);
   md.h = reinterpret_cast<float*>(base + SL.h);

@@ -73,9 +73,9 @@ static_assert(kMaxT + kMaxDraft - 1 <= kChunk, "draft positions of one step");
 enum Prologue : int32_t { PRO_RMS_X = 0, PRO_GDN_OUT = 1, PRO_FA_OUT = 2, PRO_H = 3, PRO_MTP_IN = 4 };
 enum ZeroBuf : int32_t { ZERO_NONE = 0, ZERO_GU = 1, ZERO_YIN = 2 };
 // Outputs of one GEMM phase: input projections into yin, residual add into x
-// (then the 32-wide sums of squares for the next RMSNorm), gate/up pairs into
-// gu (the SwiGLU is applied by the down projection's prologue), logits into
-// the per-warp top-1 records.
+// (red.add; the next RMSNorm sums the squares of the full rows itself), gate/up
+// pairs into gu (the SwiGLU is applied by the down projection's prologue),
+// logits into the per-warp top-1 records.
 enum Epilogue : int32_t { EPI_STORE_YIN = 0, EPI_RESID_X = 1, EPI_STORE_GU = 2, EPI_TOP2 = 3 };
 
 struct GemmDesc {
@@ -135,7 +135,6 @@ struct ModelDesc {
   int32_t img_k;
   int32_t pad_img;
   float* x;          // [kMaxRows][H] residual stream
-  float* xsq;        // [H/32][kMaxRows] sums of squares of x over each 32-wide chunk
   float* yin;        // [kMaxRows][n_in_max] input projections
   float* o;          // [kMaxRows][o_stride] mixer outputs
   float* h;          // [kMaxRows][F] SwiGLU output (written only while debug outputs are on)

@@ -319,7 +319,6 @@ __device__ void embed_phase(const ModelDesc& md, const StepDesc& sd, const WarpC
     const float sc = static_cast<float>((lo64 >> (6 * j)) & 63u);
     const float m = static_cast<float>((mid64 >> (16 + 6 * j)) & 63u);
     const float ds = d * sc, dm = dmin * m;
-    float sq = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int i = i0 + e;
@@ -327,12 +326,7 @@ __device__ void embed_phase(const ModelDesc& md, const StepDesc& sd, const WarpC
       const int q = i < 16 ? (byte & 15) : (byte >> 4);
       const float xv = ds * static_cast<float>(q) - dm;
       md.x[static_cast<size_t>(r) * md.H + sb * 256 + 32 * j + i] = xv;
-      sq = fmaf(xv, xv, sq);
     }
-    // the 4 lanes of sub-block j hold one 32-wide chunk
-    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-    if ((wc.lane & 3) == 0) md.xsq[static_cast<size_t>(sb * 8 + j) * kMaxRows + r] = sq;
   }
 }
 
@@ -374,12 +368,57 @@ __device__ __forceinline__ void put_act(__half* act, int cs2, int R, float* sx, 
   if ((lane & 7) == 0) sx[((kl >> 8) * 8 + ((kl & 255) >> 5)) * R + r] = part;
 }
 
+// 1/rms of every row of the residual stream into misc[r], from the full rows
+// (the residual writers only add into x, so nobody else has the sums): the
+// loads of a batch are all issued before any is used, with the batch sized to
+// the row count (one batch for one row group of 4 at the 27B width).
+template <int NT>
+__device__ __forceinline__ void row_inv_rms(const ModelDesc& md, int R, float* misc, float* red) {
+  constexpr int RB = 4 * NT, JB = NT == 1 ? 6 : NT == 2 ? 3 : 2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nq4 = md.H / 4;
+  float sq[RB];
+#pragma unroll
+  for (int r = 0; r < RB; ++r) sq[r] = 0.f;
+  for (int j0 = 0; j0 * kThreads < nq4; j0 += JB) {
+    float4 v[RB][JB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj) {
+        const int c = (j0 + jj) * kThreads + tid;
+        v[r][jj] = (r < R && c < nq4)
+                       ? __ldcg(reinterpret_cast<const float4*>(md.x + static_cast<size_t>(r) * md.H) + c)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj)
+        sq[r] = fmaf(v[r][jj].x, v[r][jj].x, fmaf(v[r][jj].y, v[r][jj].y,
+                     fmaf(v[r][jj].z, v[r][jj].z, fmaf(v[r][jj].w, v[r][jj].w, sq[r]))));
+  }
+#pragma unroll
+  for (int r = 0; r < RB; ++r)
+    if (r < R) {
+      const float t = warp_sum(sq[r]);
+      if (lane == 0) red[warp * kMaxRows + r] = t;
+    }
+  math_sync();
+  if (tid < R) {
+    float t = 0.f;
+    for (int w = 0; w < kWarps; ++w) t += red[w * kMaxRows + tid];
+    misc[tid] = 1.0f / sqrtf(t / static_cast<float>(md.H) + md.eps);
+  }
+  math_sync();
+}
+
 // One round of loads: every thread issues all of its source float4 loads
-// (up to kB groups, plus the per-chunk sums of squares for an RMSNorm) before
-// using any of them, so the prologue costs about one L2 round trip.
-// RMSNorm: 1/rms from the 32-wide chunk sums the residual writers left, added
-// in a fixed order. Gated DeltaNet output: each head's 128 (or 64) values are
-// the float4s of 32 (or 16) consecutive lanes, so its norm is a shuffle sum.
+// (up to kB groups) before using any of them, so the prologue costs about
+// one L2 round trip (plus the row norms' batches for an RMSNorm).
+// Gated DeltaNet output: each head's 128 (or 64) values are the float4s of
+// 32 (or 16) consecutive lanes, so its norm is a shuffle sum.
+template <int NT>
 __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g, int sb0,
                               int nsb_s, const Smem& sm) {
   constexpr int kB = 8;
@@ -394,11 +433,10 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
   const int per_row = ks / 4;
   const int cs2 = cstride / 2;
   const int total = R * per_row;
-  const int nchunk = md.H / 32;
+  if (g.pro == PRO_RMS_X) row_inv_rms<NT>(md, R, misc, red);
   for (int base = 0; base < total; base += kThreads * kB) {
     // every source of this round, norm gains included, is loaded before any is used
     float4 s1[kB], s2[kB], s3[kB];
-    float sq[kMaxRows];
 #pragma unroll
     for (int b = 0; b < kB; ++b) {
       const int idx = base + b * kThreads + tid;
@@ -423,27 +461,6 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
           s2[b] = __ldcg(reinterpret_cast<const float4*>(gr + 8));
         }
       }
-    }
-    if (g.pro == PRO_RMS_X && base == 0) {
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        sq[r] = 0.f;
-        if (r < R)
-          for (int c = tid; c < nchunk; c += kThreads) sq[r] += __ldcg(md.xsq + static_cast<size_t>(c) * kMaxRows + r);
-      }
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r)
-        if (r < R) {
-          const float t = warp_sum(sq[r]);
-          if (lane == 0) red[warp * kMaxRows + r] = t;
-        }
-      math_sync();
-      if (tid < R) {
-        float t = 0.f;
-        for (int w = 0; w < kWarps; ++w) t += red[w * kMaxRows + tid];
-        misc[tid] = 1.0f / sqrtf(t / static_cast<float>(md.H) + md.eps);
-      }
-      math_sync();
     }
 #pragma unroll
     for (int b = 0; b < kB; ++b) {
@@ -501,8 +518,8 @@ __device__ __forceinline__ float* top_rec(int warp) {
 // v[r] is the complete output of the lane's row n = 32 tile + lane for
 // activation row r. For a tile that several warps computed, the outputs were
 // summed in global memory (red.add into the phase's output buffer) and v was
-// read back from there: `summed` marks that case (then x already holds the
-// residual sum and yin needs nothing more).
+// read back from there: `summed` marks that case (then the stores need
+// nothing more). Residual adds never come here: every warp red.adds its part.
 template <int NT, bool TOP>
 __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g,
                                               uint32_t tile, const float (&v)[4 * NT], int lane, int warp,
@@ -517,22 +534,8 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
           if (r < R) md.yin[static_cast<size_t>(r) * md.n_in_max + n] = v[r];
       }
       break;
-    case EPI_RESID_X: {
-      // H is a multiple of 256, so every lane of the tile holds a real row
-#pragma unroll
-      for (int r = 0; r < 4 * NT; ++r)
-        if (r < R) {
-          float* p = md.x + static_cast<size_t>(r) * md.H + n;
-          float xn = v[r];
-          if (!summed) {
-            xn += __ldcg(p);
-            *p = xn;
-          }
-          const float sq = warp_sum(xn * xn);  // the next RMSNorm's partial for this 32-wide chunk
-          if (lane == 0) md.xsq[static_cast<size_t>(tile) * kMaxRows + r] = sq;
-        }
+    case EPI_RESID_X:  // added into x by red.add in the flush; nothing completes here
       break;
-    }
     case EPI_STORE_GU:
       if (!summed && n < g.n_out) {
 #pragma unroll
@@ -640,7 +643,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
     const int cols = g.zero_buf == ZERO_GU ? 2 * md.F : md.n_in_max;
     for (int idx = blockIdx.x * kThreads + threadIdx.x; idx < R * cols; idx += grid * kThreads) zp[idx] = 0.f;
   }
-  gemm_prologue(md, sd, g, a.sb0, a.nsb_s, sm);
+  gemm_prologue<NT>(md, sd, g, a.sb0, a.nsb_s, sm);
 
   const int lane = wc.lane, gq = lane >> 2, cq = lane & 3;
   const int cstride = act_col_stride(a.nsb_s);
@@ -660,9 +663,10 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
   float* dst = g.epi == EPI_STORE_YIN ? md.yin : g.epi == EPI_RESID_X ? md.x : g.epi == EPI_STORE_GU ? md.gu : md.logits;
   const int dstride = g.epi == EPI_STORE_YIN ? md.n_in_max : g.epi == EPI_RESID_X ? md.H
                       : g.epi == EPI_STORE_GU ? 2 * md.F : md.V;
-  // stores and split logits need no completion step: the summed buffer is the
-  // output (split logits are scanned by lm_argmax after the next barrier)
-  const bool no_ticket = g.epi == EPI_STORE_YIN || g.epi == EPI_STORE_GU || (TOP && a.sc.S > 1);
+  // stores, residual adds and split logits need no completion step: the
+  // summed buffer is the output (the next RMSNorm takes its row sums from the
+  // full rows; split logits are scanned by lm_argmax after the next barrier)
+  const bool no_ticket = g.epi == EPI_STORE_YIN || g.epi == EPI_STORE_GU || g.epi == EPI_RESID_X || (TOP && a.sc.S > 1);
   if (TOP) {
     float* rec = top_rec(wc.warp);
     if (lane < R) {
@@ -700,7 +704,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
     for (int r = 0; r < 4 * NT; ++r) v[r] = r < R ? stage[lane * 17 + r] - mn[r] : 0.f;
     __syncwarp();
     const uint32_t tu0 = tile * nsb_s, tu1 = tu0 + nsb_s;
-    if (a.sc.S == 1 && seg_u0 == tu0 && u_end == tu1) {  // the whole tile: no one else contributes
+    if (a.sc.S == 1 && seg_u0 == tu0 && u_end == tu1 && g.epi != EPI_RESID_X) {  // the whole tile: no one else contributes
       gemm_epilogue<NT, TOP>(md, sd, g, tile, v, lane, wc.warp, false);
       return;
     }
