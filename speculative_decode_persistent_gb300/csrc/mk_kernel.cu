@@ -433,7 +433,10 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
   const int per_row = ks / 4;
   const int cs2 = cstride / 2;
   const int total = R * per_row;
-  if (g.pro == PRO_RMS_X) row_inv_rms<NT>(md, R, misc, red);
+  // one row whose whole reduction fits one round: the round's own loads are
+  // the full row, so its sum of squares comes from them (no separate batch)
+  const bool own_norm = g.pro == PRO_RMS_X && R == 1 && k0 == 0 && ks == md.H && total <= kThreads * kB;
+  if (g.pro == PRO_RMS_X && !own_norm) row_inv_rms<NT>(md, R, misc, red);
   for (int base = 0; base < total; base += kThreads * kB) {
     // every source of this round, norm gains included, is loaded before any is used
     float4 s1[kB], s2[kB], s3[kB];
@@ -461,6 +464,21 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
           s2[b] = __ldcg(reinterpret_cast<const float4*>(gr + 8));
         }
       }
+    }
+    if (own_norm) {
+      float sq = 0.f;
+#pragma unroll
+      for (int b = 0; b < kB; ++b)  // elements past the row were loaded as zeros
+        sq = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, fmaf(s1[b].w, s1[b].w, sq))));
+      sq = warp_sum(sq);
+      if (lane == 0) red[warp * kMaxRows] = sq;
+      math_sync();
+      if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < kWarps; ++w) t += red[w * kMaxRows];
+        misc[0] = 1.0f / sqrtf(t / static_cast<float>(md.H) + md.eps);
+      }
+      math_sync();
     }
 #pragma unroll
     for (int b = 0; b < kB; ++b) {
