@@ -418,12 +418,99 @@ __device__ __forceinline__ void row_inv_rms(const ModelDesc& md, int R, float* m
 // one L2 round trip (plus the row norms' batches for an RMSNorm).
 // Gated DeltaNet output: each head's 128 (or 64) values are the float4s of
 // 32 (or 16) consecutive lanes, so its norm is a shuffle sum.
+// One prologue kind's rounds, as its own straight-line code: a phase runs one
+// kind, so the instructions it executes are contiguous.
+template <int PRO>
+__device__ __forceinline__ void prologue_rounds(const ModelDesc& md, const GemmDesc& g, int R, int k0, int per_row,
+                                                __half* act, int cs2, float* sx, float* misc, float* red,
+                                                bool own_norm) {
+  constexpr int kB = 8;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int total = R * per_row;
+  for (int base = 0; base < total; base += kThreads * kB) {
+    // every source of this round, norm gains included, is loaded before any is used
+    float4 s1[kB], s2[kB], s3[kB];
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int idx = base + b * kThreads + tid;
+      s1[b] = s2[b] = s3[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (idx < total) {
+        const int r = idx / per_row, k = k0 + (idx - r * per_row) * 4;
+        if constexpr (PRO == PRO_RMS_X) {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.x + static_cast<size_t>(r) * md.H + k));
+          s2[b] = *reinterpret_cast<const float4*>(g.gain + k);
+        } else if constexpr (PRO == PRO_GDN_OUT) {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
+          s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.conv_ch + k));
+          s3[b] = *reinterpret_cast<const float4*>(g.gain + k % md.dv);
+        } else if constexpr (PRO == PRO_FA_OUT) {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
+          s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.hq * md.dh + k));
+        } else if constexpr (PRO == PRO_MTP_IN) {
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.mtp_in + static_cast<size_t>(r) * 2 * md.H + k));
+        } else {  // SwiGLU of the gate/up pair: 4 consecutive f share one 8-row block
+          const float* gr = md.gu + static_cast<size_t>(r) * 2 * md.F + (k >> 3) * 16 + (k & 7);
+          s1[b] = __ldcg(reinterpret_cast<const float4*>(gr));
+          s2[b] = __ldcg(reinterpret_cast<const float4*>(gr + 8));
+        }
+      }
+    }
+    if constexpr (PRO == PRO_RMS_X) {
+      if (own_norm) {
+        float sq = 0.f;
+#pragma unroll
+        for (int b = 0; b < kB; ++b)  // elements past the row were loaded as zeros
+          sq = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, fmaf(s1[b].w, s1[b].w, sq))));
+        sq = warp_sum(sq);
+        if (lane == 0) red[warp * kMaxRows] = sq;
+        math_sync();
+        if (tid == 0) {
+          float t = 0.f;
+          for (int w = 0; w < kWarps; ++w) t += red[w * kMaxRows];
+          misc[0] = 1.0f / sqrtf(t / static_cast<float>(md.H) + md.eps);
+        }
+        math_sync();
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int idx = base + b * kThreads + tid;
+      if (idx < total) {  // warp-uniform: total is a multiple of 64
+        const int r = idx / per_row, kl = (idx - r * per_row) * 4, k = k0 + kl;
+        float u[4];
+        if constexpr (PRO == PRO_RMS_X) {
+          const float4 gg = s2[b];
+          const float sc = misc[r];
+          u[0] = s1[b].x * sc * gg.x; u[1] = s1[b].y * sc * gg.y; u[2] = s1[b].z * sc * gg.z; u[3] = s1[b].w * sc * gg.w;
+        } else if constexpr (PRO == PRO_GDN_OUT) {
+          float hs = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, s1[b].w * s1[b].w)));
+          for (int off = 1; off < md.dv / 4; off <<= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
+          const float sc = 1.0f / sqrtf(hs / static_cast<float>(md.dv) + md.eps);
+          const float4 gg = s3[b];
+          u[0] = s1[b].x * sc * gg.x * siluf_(s2[b].x); u[1] = s1[b].y * sc * gg.y * siluf_(s2[b].y);
+          u[2] = s1[b].z * sc * gg.z * siluf_(s2[b].z); u[3] = s1[b].w * sc * gg.w * siluf_(s2[b].w);
+        } else if constexpr (PRO == PRO_FA_OUT) {
+          u[0] = s1[b].x * sigmoidf_(s2[b].x); u[1] = s1[b].y * sigmoidf_(s2[b].y);
+          u[2] = s1[b].z * sigmoidf_(s2[b].z); u[3] = s1[b].w * sigmoidf_(s2[b].w);
+        } else if constexpr (PRO == PRO_MTP_IN) {
+          u[0] = s1[b].x; u[1] = s1[b].y; u[2] = s1[b].z; u[3] = s1[b].w;
+        } else {
+          u[0] = siluf_(s1[b].x) * s2[b].x; u[1] = siluf_(s1[b].y) * s2[b].y;
+          u[2] = siluf_(s1[b].z) * s2[b].z; u[3] = siluf_(s1[b].w) * s2[b].w;
+          if (md.dbg_logits)  // debug outputs on: keep the SwiGLU rows for mk_debug_scratch
+            *reinterpret_cast<float4*>(md.h + static_cast<size_t>(r) * md.F + k) = make_float4(u[0], u[1], u[2], u[3]);
+        }
+        put_act(act, cs2, R, sx, r, kl, u, lane);
+      }
+    }
+  }
+}
+
 template <int NT>
 __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g, int sb0,
                               int nsb_s, const Smem& sm) {
   constexpr int kB = 8;
   const int R = sd.R;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = sb0 * 256, ks = nsb_s * 256;
   const int cstride = act_col_stride(nsb_s);
   __half* act = reinterpret_cast<__half*>(sm.act());
@@ -437,80 +524,12 @@ __device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const Gem
   // the full row, so its sum of squares comes from them (no separate batch)
   const bool own_norm = g.pro == PRO_RMS_X && R == 1 && k0 == 0 && ks == md.H && total <= kThreads * kB;
   if (g.pro == PRO_RMS_X && !own_norm) row_inv_rms<NT>(md, R, misc, red);
-  for (int base = 0; base < total; base += kThreads * kB) {
-    // every source of this round, norm gains included, is loaded before any is used
-    float4 s1[kB], s2[kB], s3[kB];
-#pragma unroll
-    for (int b = 0; b < kB; ++b) {
-      const int idx = base + b * kThreads + tid;
-      s1[b] = s2[b] = s3[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (idx < total) {
-        const int r = idx / per_row, k = k0 + (idx - r * per_row) * 4;
-        if (g.pro == PRO_RMS_X) {
-          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.x + static_cast<size_t>(r) * md.H + k));
-          s2[b] = *reinterpret_cast<const float4*>(g.gain + k);
-        } else if (g.pro == PRO_GDN_OUT) {
-          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
-          s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.conv_ch + k));
-          s3[b] = *reinterpret_cast<const float4*>(g.gain + k % md.dv);
-        } else if (g.pro == PRO_FA_OUT) {
-          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.o + static_cast<size_t>(r) * md.o_stride + k));
-          s2[b] = __ldcg(reinterpret_cast<const float4*>(md.yin + static_cast<size_t>(r) * md.n_in_max + md.hq * md.dh + k));
-        } else if (g.pro == PRO_MTP_IN) {
-          s1[b] = __ldcg(reinterpret_cast<const float4*>(md.mtp_in + static_cast<size_t>(r) * 2 * md.H + k));
-        } else {  // SwiGLU of the gate/up pair: 4 consecutive f share one 8-row block
-          const float* gr = md.gu + static_cast<size_t>(r) * 2 * md.F + (k >> 3) * 16 + (k & 7);
-          s1[b] = __ldcg(reinterpret_cast<const float4*>(gr));
-          s2[b] = __ldcg(reinterpret_cast<const float4*>(gr + 8));
-        }
-      }
-    }
-    if (own_norm) {
-      float sq = 0.f;
-#pragma unroll
-      for (int b = 0; b < kB; ++b)  // elements past the row were loaded as zeros
-        sq = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, fmaf(s1[b].w, s1[b].w, sq))));
-      sq = warp_sum(sq);
-      if (lane == 0) red[warp * kMaxRows] = sq;
-      math_sync();
-      if (tid == 0) {
-        float t = 0.f;
-        for (int w = 0; w < kWarps; ++w) t += red[w * kMaxRows];
-        misc[0] = 1.0f / sqrtf(t / static_cast<float>(md.H) + md.eps);
-      }
-      math_sync();
-    }
-#pragma unroll
-    for (int b = 0; b < kB; ++b) {
-      const int idx = base + b * kThreads + tid;
-      if (idx < total) {  // warp-uniform: total is a multiple of 64
-        const int r = idx / per_row, kl = (idx - r * per_row) * 4, k = k0 + kl;
-        float u[4];
-        if (g.pro == PRO_RMS_X) {
-          const float4 gg = s2[b];
-          const float sc = misc[r];
-          u[0] = s1[b].x * sc * gg.x; u[1] = s1[b].y * sc * gg.y; u[2] = s1[b].z * sc * gg.z; u[3] = s1[b].w * sc * gg.w;
-        } else if (g.pro == PRO_GDN_OUT) {
-          float hs = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, s1[b].w * s1[b].w)));
-          for (int off = 1; off < md.dv / 4; off <<= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
-          const float sc = 1.0f / sqrtf(hs / static_cast<float>(md.dv) + md.eps);
-          const float4 gg = s3[b];
-          u[0] = s1[b].x * sc * gg.x * siluf_(s2[b].x); u[1] = s1[b].y * sc * gg.y * siluf_(s2[b].y);
-          u[2] = s1[b].z * sc * gg.z * siluf_(s2[b].z); u[3] = s1[b].w * sc * gg.w * siluf_(s2[b].w);
-        } else if (g.pro == PRO_FA_OUT) {
-          u[0] = s1[b].x * sigmoidf_(s2[b].x); u[1] = s1[b].y * sigmoidf_(s2[b].y);
-          u[2] = s1[b].z * sigmoidf_(s2[b].z); u[3] = s1[b].w * sigmoidf_(s2[b].w);
-        } else if (g.pro == PRO_MTP_IN) {
-          u[0] = s1[b].x; u[1] = s1[b].y; u[2] = s1[b].z; u[3] = s1[b].w;
-        } else {
-          u[0] = siluf_(s1[b].x) * s2[b].x; u[1] = siluf_(s1[b].y) * s2[b].y;
-          u[2] = siluf_(s1[b].z) * s2[b].z; u[3] = siluf_(s1[b].w) * s2[b].w;
-          if (md.dbg_logits)  // debug outputs on: keep the SwiGLU rows for mk_debug_scratch
-            *reinterpret_cast<float4*>(md.h + static_cast<size_t>(r) * md.F + k) = make_float4(u[0], u[1], u[2], u[3]);
-        }
-        put_act(act, cs2, R, sx, r, kl, u, lane);
-      }
-    }
+  switch (g.pro) {
+    case PRO_RMS_X: prologue_rounds<PRO_RMS_X>(md, g, R, k0, per_row, act, cs2, sx, misc, red, own_norm); break;
+    case PRO_GDN_OUT: prologue_rounds<PRO_GDN_OUT>(md, g, R, k0, per_row, act, cs2, sx, misc, red, false); break;
+    case PRO_FA_OUT: prologue_rounds<PRO_FA_OUT>(md, g, R, k0, per_row, act, cs2, sx, misc, red, false); break;
+    case PRO_MTP_IN: prologue_rounds<PRO_MTP_IN>(md, g, R, k0, per_row, act, cs2, sx, misc, red, false); break;
+    default: prologue_rounds<PRO_H>(md, g, R, k0, per_row, act, cs2, sx, misc, red, false); break;
   }
   math_sync();
 }
@@ -993,7 +1012,7 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
       float sq[kMaxT], sk[kMaxT];
   #pragma unroll
       for (int t = 0; t < kMaxT; ++t) sq[t] = sk[t] = 0.f;
-  #pragma unroll
+  #pragma unroll 1
       for (int e = 0; e < 4; ++e) {
         if (e < ne) {
           const int d = lane + 32 * e;
