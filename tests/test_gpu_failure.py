@@ -43,3 +43,29 @@ def test_host_side_errors(cuda_ok):
         p.eng.step(long_tok, np.arange(64, 76), np.zeros(12, np.int32))
     ro, rg = p.step(tok, pos, sid)
     p.compare_step(ro, rg, sid)
+
+
+@pytest.mark.parametrize("barrier", [26, 31, 35])
+def test_barrier_timeout_inside_draft_passes(cuda_ok, barrier):
+    """The same recovery when the skipped arrival falls inside the MTP head's
+    passes. On the 4-layer model the main step uses barriers 0..22 (22 closes
+    verify); each draft pass then has nine. 26 is pass 0's attention, 31 its
+    draft phase, and 35 the attention of pass 1, which reads back earlier
+    draft positions."""
+    from speculative_decode_persistent_gb300 import mk
+    from gen import configs
+    model = dict(configs.TINY, has_mtp=1, draft_vocab=1024)
+    p = Pair("tiny", overrides=dict(model=model, n_draft=3, n_pages=72))
+    tok, pos, sid = p.wl.rows([[1, 2, 3]])
+    p.eng.skip_arrival(block=3, barrier=barrier, timeout_ns=50_000_000)
+    with pytest.raises(mk.MkError) as e:
+        p.eng.step(tok, pos, sid)
+    assert e.value.status == -4
+    with pytest.raises(mk.MkError) as e:
+        p.eng.last_drafts(1)
+    assert e.value.status == -1  # no drafts from a failed step
+    p.eng.skip_arrival(-1, -1, 0)
+    ro, rg = p.step(tok, pos, sid)
+    p.compare_step(ro, rg, sid)
+    co, cg = int(ro["counts"][0]), int(rg["counts"][0])
+    p.compare_drafts([0], [co == cg])
