@@ -851,6 +851,9 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
     c->step_T[i] = T[i];
   }
   sd.n_attn_items = items;
+  // the splits of one (sequence, kv head) wait for each other before merging:
+  // every item needs a block of its own
+  if (items > c->grid) return MK_ERR_UNSUPPORTED;
   if (L.fa_dh > 0) {
     attn_plan(t_max * (L.fa_hq / hkv), L.fa_dh, L.kv_dtype == MK_KV_Q8, kRingBytes, sd.attn_dsplit, sd.attn_wpg,
               sd.attn_ng, sd.attn_spg, sd.attn_nslots);
@@ -880,8 +883,10 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
 
 mk_status mk_step_launch(mk_ctx* c) {
   if (!c || !c->prepared) return MK_ERR_INVALID;
+  // the barrier counter and the attention split counters count up within one launch
   if (cudaMemsetAsync(c->md_host.bar, 0, 64, c->stream) != cudaSuccess ||
-      cudaMemsetAsync(c->md_host.err, 0, 64, c->stream) != cudaSuccess)
+      cudaMemsetAsync(c->md_host.err, 0, 64, c->stream) != cudaSuccess ||
+      cudaMemsetAsync(c->md_host.attn_tickets, 0, c->attn_tickets_bytes, c->stream) != cudaSuccess)
     return MK_ERR_CUDA;
   cudaEventRecord(c->ev0, c->stream);
   const cudaError_t e =

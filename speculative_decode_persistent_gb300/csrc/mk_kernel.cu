@@ -1547,25 +1547,46 @@ constexpr int kAttnQBytes = (kMaxQRows * (kMaxDh + 8) * 2 + 255) / 256 * 256;
 constexpr int kAttnNewBytes = 16384;                          // largest slot (fp16, dh 256)
 constexpr int kAttnMergeBytes = 4 * (4 + 4 * (kMaxDh / 16)) * 32 * 4;  // worst plan: 1 x 4 warps, 16 m-tiles
 static_assert(kAttnQBytes + kAttnNewBytes + kAttnMergeBytes + 16 <= kPhaseBytes, "attention shared memory");
-static_assert(kWarps * kMaxSplits * 4 <= kAttnMergeBytes, "attention combine weights");
+static_assert((2 * kMaxQRows * kMaxSplits + kMaxQRows) * 4 <= kAttnQBytes + kAttnNewBytes + kAttnMergeBytes,
+              "attention combine scratch (below the phase's flag word)");
 static_assert(kAttnBarOff + 2 * kAttnMaxSlots * 8 <= kMiscBytes, "attention mbarriers");
 
-// The last block of a (sequence, kv head) merges the splits' partials with
-// all its math threads: split weights 2^(m_s - M) per query row into shared
-// memory, then one thread per (query row, 4 head dims) sums the splits with
-// 16-byte loads, several in flight.
+// Every block of a (sequence, kv head) merges its share of the splits'
+// partials once all of them are written: split j takes the output float4s
+// j, j + nsplit, ... of the head's [qrows][dh/4] output. First every split's
+// (m, l) of every row goes to shared memory in one batch of loads; then per
+// row the weights 2^(m_s - M) and 1/sum(l_s w_s); then groups of 4 threads sum
+// one output float4 over the splits (each thread a quarter of them, all its
+// loads in flight) and a shuffle adds the four.
 __device__ __noinline__ void attn_combine(const ModelDesc& md, const StepDesc& sd, int si, int kh, int nsplit,
-                                          int qrows, int row0, float* wsm) {
+                                          int qrows, int row0, int j, float* wsm) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int dh = md.dh, grp = md.hq / md.hkv;
-  __threadfence();
   const int item0 = sd.seq_item0[si] + kh * nsplit;
-  float* wm = wsm;                    // [qrows][nsplit]: m, then the weight
-  float* inv = wsm + qrows * nsplit;  // [qrows]
+  const int n = qrows * nsplit;
+  float* wm = wsm;          // [qrows][nsplit]: m, then the weight
+  float* wl = wsm + n;      // [qrows][nsplit]: l
+  float* inv = wsm + 2 * n;  // [qrows]
   auto part = [&](int sp, int r) {
     return md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + r) * kPartStride;
   };
-  for (int idx = tid; idx < qrows * nsplit; idx += kThreads) wm[idx] = __ldcg(part(idx % nsplit, idx / nsplit) + kMaxDh);
+  for (int base = 0; base < n; base += kThreads * 8) {
+    float2 ml[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int idx = base + b * kThreads + tid;
+      ml[b] = idx < n ? __ldcg(reinterpret_cast<const float2*>(part(idx % nsplit, idx / nsplit) + kMaxDh))
+                      : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int idx = base + b * kThreads + tid;
+      if (idx < n) {
+        wm[idx] = ml[b].x;
+        wl[idx] = ml[b].y;
+      }
+    }
+  }
   math_sync();
   for (int r = warp; r < qrows; r += kWarps) {
     float mloc = -INFINITY;
@@ -1576,29 +1597,76 @@ __device__ __noinline__ void attn_combine(const ModelDesc& md, const StepDesc& s
       const float ms = wm[r * nsplit + sp];
       const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
       wm[r * nsplit + sp] = w;
-      lloc = fmaf(__ldcg(part(sp, r) + kMaxDh + 1), w, lloc);
+      lloc = fmaf(wl[r * nsplit + sp], w, lloc);
     }
     const float tot = warp_sum(lloc);
     if (lane == 0) inv[r] = 1.0f / tot;
   }
   math_sync();
-  const int d4n = dh / 4;
-  for (int idx = tid; idx < qrows * d4n; idx += kThreads) {
-    const int r = idx / d4n, d4 = idx - r * d4n;
+  const int d4n = dh / 4, total = qrows * d4n;
+  constexpr int kG = 4;                     // threads per output float4
+  constexpr int kSlots = kThreads / kG;     // outputs per pass of the block
+  const int q = tid & (kG - 1), slot = tid / kG;
+  // the pass loop is warp-uniform (the shuffles below need the whole warp)
+  for (int pass = 0; j + nsplit * (warp * (32 / kG) + kSlots * pass) < total; ++pass) {
+    const int o = j + nsplit * (slot + kSlots * pass);
+    const bool valid = o < total;
+    const int r = valid ? o / d4n : 0, d4 = valid ? o - r * d4n : 0;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(part(sp, r)) + d4);
-      const float w = wm[r * nsplit + sp];
-      a.x = fmaf(w, v.x, a.x);
-      a.y = fmaf(w, v.y, a.y);
-      a.z = fmaf(w, v.z, a.z);
-      a.w = fmaf(w, v.w, a.w);
+    for (int sp0 = q; sp0 < nsplit; sp0 += kG * 16) {
+      float4 v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int sp = sp0 + kG * u;
+        v[u] = (valid && sp < nsplit) ? __ldcg(reinterpret_cast<const float4*>(part(sp, r)) + d4)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int sp = sp0 + kG * u;
+        const float w = (valid && sp < nsplit) ? wm[r * nsplit + sp] : 0.f;
+        a.x = fmaf(w, v[u].x, a.x);
+        a.y = fmaf(w, v[u].y, a.y);
+        a.z = fmaf(w, v[u].z, a.z);
+        a.w = fmaf(w, v[u].w, a.w);
+      }
     }
-    const float iv = inv[r];
-    const int t = r / grp, hh = kh * grp + r % grp;
-    float4* o = reinterpret_cast<float4*>(md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh) + d4;
-    *o = make_float4(a.x * iv, a.y * iv, a.z * iv, a.w * iv);
+#pragma unroll
+    for (int off = 1; off < kG; off <<= 1) {
+      a.x += __shfl_xor_sync(0xffffffffu, a.x, off);
+      a.y += __shfl_xor_sync(0xffffffffu, a.y, off);
+      a.z += __shfl_xor_sync(0xffffffffu, a.z, off);
+      a.w += __shfl_xor_sync(0xffffffffu, a.w, off);
+    }
+    if (valid && q == 0) {
+      const float iv = inv[r];
+      const int t = r / grp, hh = kh * grp + r % grp;
+      float4* op = reinterpret_cast<float4*>(md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh) + d4;
+      *op = make_float4(a.x * iv, a.y * iv, a.z * iv, a.w * iv);
+    }
+  }
+}
+
+// Bounded wait until every split of (sequence, kv head) `key` has announced
+// its partial for attention phase number `ord` of this launch: the counter
+// only grows within a launch (the host clears it before each), so the phase's
+// target is (ord + 1) x nsplit. False (and the error word set) on timeout or
+// when another block has already reported an error.
+__device__ bool attn_splits_ready(const ModelDesc& md, const StepDesc& sd, int key, int ord, int nsplit) {
+  const uint32_t target = static_cast<uint32_t>(ord + 1) * static_cast<uint32_t>(nsplit);
+  volatile int32_t* err = md.err;
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire(md.attn_tickets + key) >= target) return true;
+    if ((it & 31u) == 31u) {
+      if (*err != 0) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > sd.barrier_timeout_ns || it > (1u << 30)) {
+        atomicCAS(md.err, 0, DEV_BARRIER_TIMEOUT);
+        return false;
+      }
+    }
   }
 }
 
@@ -1643,24 +1711,47 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
 
     // Q (RoPE, 1/sqrt(dh), binary16), head dims in the order the K fragments
     // present them; rows past qrows are zero
-    for (int idx = tid; idx < nq * 8 * (dh / 2); idx += kThreads) {
-      const int qr = idx / (dh / 2), pp = 2 * (idx % (dh / 2));
-      const int sidx = pp >> 4, l16 = pp & 15, j = sidx >> 1, h = sidx & 1, cc = (l16 & 7) >> 1, hi = l16 >> 3;
-      const int d = Q8 ? 32 * j + 8 * cc + 4 * h + 2 * hi : 64 * (j >> 1) + 16 * cc + 8 * (j & 1) + 4 * h + 2 * hi;
-      float v0 = 0.f, v1 = 0.f;
-      if (qr < qrows) {
-        const int t = qr / grp, hh = kh * grp + qr % grp, row = row0 + t;
+    // batches of 4 pairs per thread: all of a batch's loads are issued before
+    // its shared-memory stores
+    const int nqe = nq * 8 * (dh / 2);
+    for (int base = 0; base < nqe; base += kThreads * 4) {
+      float qa[4][2], qb[4][2];
+      float2 qc[4][2];
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int idx = base + bb * kThreads + tid;
+        const int qr = idx / (dh / 2), pp = 2 * (idx % (dh / 2));
+        const int sidx = pp >> 4, l16 = pp & 15, j = sidx >> 1, h = sidx & 1, cc = (l16 & 7) >> 1, hi = l16 >> 3;
+        const int d = Q8 ? 32 * j + 8 * cc + 4 * h + 2 * hi : 64 * (j >> 1) + 16 * cc + 8 * (j & 1) + 4 * h + 2 * hi;
+        const bool in = idx < nqe && qr < qrows;
+        const int t = in ? qr / grp : 0, hh = kh * grp + (in ? qr % grp : 0), row = row0 + t;
         const float* q = md.yin + static_cast<size_t>(row) * md.n_in_max + hh * dh;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int dd = d + e, i = dd % (dh / 2);
-          const float a = __ldcg(q + i), b = __ldcg(q + i + dh / 2);
-          const float2 cs = mp ? __ldcg(md.mtp_rope + si * (kMaxDh / 2) + i) : sd.rope[row][i];
-          const float v = (dd < dh / 2 ? a * cs.x - b * cs.y : a * cs.y + b * cs.x) * q_scale;
-          if (e == 0) v0 = v; else v1 = v;
+          const int i = (d + e) % (dh / 2);
+          qa[bb][e] = in ? __ldcg(q + i) : 0.f;
+          qb[bb][e] = in ? __ldcg(q + i + dh / 2) : 0.f;
+          qc[bb][e] = !in ? make_float2(0.f, 0.f)
+                          : mp ? __ldcg(md.mtp_rope + si * (kMaxDh / 2) + i) : sd.rope[row][i];
         }
       }
-      *reinterpret_cast<__half2*>(Qp + qr * qstride + pp) = __floats2half2_rn(v0, v1);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int idx = base + bb * kThreads + tid;
+        if (idx < nqe) {
+          const int qr = idx / (dh / 2), pp = 2 * (idx % (dh / 2));
+          const int sidx = pp >> 4, l16 = pp & 15, j = sidx >> 1, h = sidx & 1, cc = (l16 & 7) >> 1, hi = l16 >> 3;
+          const int d = Q8 ? 32 * j + 8 * cc + 4 * h + 2 * hi : 64 * (j >> 1) + 16 * cc + 8 * (j & 1) + 4 * h + 2 * hi;
+          float v[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float a = qa[bb][e], b = qb[bb][e];
+            const float2 cs = qc[bb][e];
+            v[e] = (d + e < dh / 2 ? a * cs.x - b * cs.y : a * cs.y + b * cs.x) * q_scale;
+          }
+          *reinterpret_cast<__half2*>(Qp + qr * qstride + pp) = __floats2half2_rn(v[0], v[1]);
+        }
+      }
     }
     // the step's own rows (last split): RoPE k, store K/V into the pool, and
     // keep the stored values as one more chunk, causal over the T rows (a
@@ -1812,17 +1903,17 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
       }
     }
     if (it.nsplit > 1) {
+      // announce this split's partial, wait for the others, merge this split's share
       __threadfence();
       math_sync();
       if (tid == 0) {
         const int key = si * hkv + kh;
-        const uint32_t old = atomicAdd(&md.attn_tickets[key], 1u);
-        const int is_last = old + 1u == static_cast<uint32_t>(it.nsplit);
-        if (is_last) md.attn_tickets[key] = 0u;
-        *flag = is_last;
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(md.attn_tickets + key) : "memory");
+        *flag = attn_splits_ready(md, sd, key, fa_i + mp, it.nsplit) ? 1 : 0;
       }
       math_sync();
-      if (*flag) attn_combine(md, sd, si, kh, it.nsplit, qrows, row0, mbuf);
+      if (*flag) attn_combine(md, sd, si, kh, it.nsplit, qrows, row0, it.j, reinterpret_cast<float*>(sm.phase()));
+      else ok = false;
     }
     math_sync();
   }
