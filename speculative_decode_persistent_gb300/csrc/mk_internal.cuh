@@ -319,8 +319,9 @@ __host__ __device__ inline Assign assign_units(int n_tiles, int nsb, int R, int 
   return a;
 }
 
-// Contributions a split tile's completion ticket waits for: one per warp
-// range holding any of its units, over every slice.
+// Contributions a split tile's completion ticket waits for (lm_head tiles
+// split across warps when its reduction is not sliced): one per warp range
+// holding any of its units, over every slice.
 __host__ __device__ inline uint32_t tile_arrivals(const Sched& sc, int n_tiles, int nsb, int grid, uint32_t tile) {
   uint32_t na = 0;
   for (int sl = 0; sl < sc.S; ++sl) {

@@ -1145,16 +1145,15 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
   }
 }
 
-// -------------------------------------------------------------- attention
-// Split-K flash decoding over the paged pool for one (sequence, kv head,
-// split): all T x (hq/hkv) query rows of the kv head share every K/V tile of
-// 32 tokens; scores and P V run on mma.sync (fp16 in, fp32 accumulate); the
-// last split also RoPEs, rounds or quantises and appends this step's own keys
-// and values, then attends to them with the causal mask across the draft
-// rows. Splits write (m, l, acc) partials; the last block to finish a
-// (sequence, head) combines them in split order.
 // ---------------------------------------------------------------- attention
-// Split-K flash decoding over the paged KV pool, transposed so that the head
+// Split-K flash decoding over the paged KV pool for one (sequence, kv head,
+// split): all T x (hq/hkv) query rows of the kv head share every K/V page.
+// The last split also RoPEs, rounds or quantises and appends this step's own
+// keys and values, then attends to them with the causal mask across the draft
+// rows. Splits write (m, l, acc) partials; once all of a (sequence, head)'s
+// splits have announced theirs, every split block merges its share.
+//
+// The mma work is transposed so that the head
 // dimension and the tokens are the mma's M and K: per 16-token chunk a warp
 // forms S^T = K Q^T (16 tokens x 8 query rows), updates the online softmax of
 // its 8 query rows, and accumulates O^T += V^T P^T (its share of the head
