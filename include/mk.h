@@ -198,7 +198,12 @@ mk_status mk_seq_get(mk_ctx* ctx, int32_t seq, int32_t* length, int32_t* pages,
  * Rows (host arrays of n_rows): rows of one sequence are contiguous, have
  * consecutive positions starting at the sequence's committed length, and
  * carry the last emitted token in the first row and draft tokens after it.
- * row_flags may be NULL (all 0); 0 = verify row. A sequence may appear once.
+ * row_flags may be NULL (all 0). 0 = verify row; 1 = prompt row (prefill:
+ * the rows are taken as given, nothing is verified); 2 = prompt row that
+ * ends its prompt (allowed only as a sequence's last row). All rows of a
+ * sequence are of one kind, at most MK_MAX_T of them per step (a longer
+ * prompt chunk takes several steps); prompt rows are refused with
+ * MK_ERR_UNSUPPORTED when the model has an MTP head. A sequence may appear once.
  * Before the launch the library commits any pending step of the sequences in
  * this step (keeping every accepted row) and allocates pages for the new
  * positions: the lowest free page id first, in row order. With an MTP head
@@ -207,8 +212,11 @@ mk_status mk_seq_get(mk_ctx* ctx, int32_t seq, int32_t* length, int32_t* pages,
  * Outputs (host): out_tokens[n_rows] receives, per sequence in order of
  * first appearance, the accepted drafts followed by the bonus token (the
  * main model's greedy choice after the last accepted row); out_counts[number
- * of sequences] receives a+1 where a is the number of accepted drafts.
- * The step leaves each sequence PENDING until mk_commit or its next step.
+ * of sequences] receives a+1 where a is the number of accepted drafts. For a
+ * sequence of prompt rows the count is 0, or 1 when its rows end the prompt
+ * (the token is the greedy choice after its last row).
+ * The step leaves each verified sequence PENDING until mk_commit or its next
+ * step; a sequence of prompt rows is committed through its last row at once.
  * Errors: MK_ERR_INVALID, MK_ERR_NO_PAGES (before any device work),
  * MK_ERR_LAUNCH, MK_ERR_BARRIER_TIMEOUT, MK_ERR_NONFINITE, MK_ERR_CUDA.
  * On a device-side error no sequence becomes pending.

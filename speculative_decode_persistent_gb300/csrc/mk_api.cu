@@ -205,6 +205,7 @@ struct mk_ctx {
   int step_seq[kMaxSeqs];
   int step_T[kMaxSeqs];
   int step_snap[kMaxSeqs][kMaxT];
+  int step_prompt[kMaxSeqs];  // 0 verify, 1 prompt rows, 2 prompt rows ending the prompt
   int skip_block = -1, skip_barrier = -1;
   uint64_t barrier_timeout_ns = 500000000ull;
   size_t tickets_bytes = 0, attn_tickets_bytes = 0;
@@ -246,6 +247,36 @@ cudaError_t upload_pages(mk_ctx* c, int seq) {
   c->h2d_bytes += s.pages.size() * sizeof(int32_t);
   return cudaMemcpyAsync(c->md_host.page_table + static_cast<size_t>(seq) * c->L.max_pages_per_seq, row,
                          s.pages.size() * sizeof(int32_t), cudaMemcpyHostToDevice, c->stream);
+}
+
+// Bookkeeping of a completed step from the result block h: verified
+// sequences become pending with their accepted count (mk_commit or the next
+// step commits); prompt rows are committed through their last row at once.
+// False when the device reported an impossible count.
+bool finish_seqs(mk_ctx* c, const int32_t* h, int32_t* out_tokens, int32_t* out_counts) {
+  int at = 0;
+  for (int i = 0; i < c->n_seq; ++i) {
+    const int cnt = h[kOutCounts + i];
+    const int T = c->step_T[i];
+    SeqInfo& s = c->seqs[c->step_seq[i]];
+    for (int t = 0; t < T; ++t) s.snap_slot[t] = c->step_snap[i][t];
+    if (c->step_prompt[i]) {
+      if (cnt != (c->step_prompt[i] == 2 ? 1 : 0)) return false;
+      s.pending = true;
+      s.count = T;
+      commit_seq(c, s, T);
+    } else {
+      if (cnt < 1 || cnt > T) return false;
+      s.pending = true;
+      s.count = cnt;
+    }
+    if (out_counts) out_counts[i] = cnt;
+    for (int k = 0; k < cnt; ++k) {
+      if (out_tokens) out_tokens[at] = h[kOutTokens + at];
+      ++at;
+    }
+  }
+  return true;
 }
 
 }  // namespace
@@ -729,9 +760,11 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
   const mk_layout& L = c->L;
   c->prepared = c->launched = false;
   // group rows into contiguous runs of one sequence each
-  int n_seq = 0, row0[kMaxSeqs], T[kMaxSeqs], sid[kMaxSeqs];
+  int n_seq = 0, row0[kMaxSeqs], T[kMaxSeqs], sid[kMaxSeqs], prompt[kMaxSeqs];
   for (int r = 0; r < n_rows; ++r) {
-    if (row_flags && row_flags[r] != 0) return MK_ERR_UNSUPPORTED;
+    const int f = row_flags ? row_flags[r] : 0;
+    if (f > 2) return MK_ERR_INVALID;
+    if (f != 0 && L.has_mtp) return MK_ERR_UNSUPPORTED;  // the MTP head runs over verified rows only
     if (tokens[r] < 0 || tokens[r] >= L.vocab) return MK_ERR_INVALID;
     const int s = seq_ids[r];
     if (s < 0 || s >= L.max_seqs || !c->seqs[s].used) return MK_ERR_INVALID;
@@ -739,7 +772,12 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
       for (int i = 0; i < n_seq; ++i)
         if (sid[i] == s) return MK_ERR_INVALID;
       if (n_seq == kMaxSeqs) return MK_ERR_INVALID;
-      sid[n_seq] = s; row0[n_seq] = r; T[n_seq] = 0; ++n_seq;
+      sid[n_seq] = s; row0[n_seq] = r; T[n_seq] = 0; prompt[n_seq] = f; ++n_seq;
+    } else {
+      // every row of a sequence is of one kind; flag 2 (ends the prompt) only on its last row
+      const int prev = prompt[n_seq - 1];
+      if ((f != 0) != (prev != 0) || prev == 2) return MK_ERR_INVALID;
+      prompt[n_seq - 1] = f;  // the sequence's kind is its last row's flag
     }
     ++T[n_seq - 1];
   }
@@ -833,7 +871,11 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
     sd.seq_T[i] = T[i];
     sd.seq_len[i] = s.len;
     sd.seq_slot_in[i] = s.slot;
-    sd.seq_snap_all[i] = 1;
+    // verify rows keep the state after every row (the commit picks one); prompt
+    // rows are committed through their last row, so only that state is written
+    sd.seq_snap_all[i] = prompt[i] ? 0 : 1;
+    sd.seq_prompt[i] = prompt[i];
+    c->step_prompt[i] = prompt[i];
     int at = 0;
     for (int t = 0; t < T[i]; ++t) {
       if (at == s.slot) ++at;
@@ -920,23 +962,10 @@ mk_status mk_step_finish(mk_ctx* c, int32_t* out_tokens, int32_t* out_counts) {
     cudaStreamSynchronize(c->stream);
     return MK_ERR_BARRIER_TIMEOUT;
   }
-  int at = 0;
   if (c->L.has_mtp)
     for (int i = 0; i < c->n_seq; ++i)
       for (int j = 0; j < c->L.n_draft; ++j) c->drafts.push_back(h[kOutDrafts + i * kMaxDraft + j]);
-  for (int i = 0; i < c->n_seq; ++i) {
-    const int cnt = h[kOutCounts + i];
-    if (cnt < 1 || cnt > c->step_T[i]) return MK_ERR_CUDA;
-    SeqInfo& s = c->seqs[c->step_seq[i]];
-    s.pending = true;
-    s.count = cnt;
-    for (int t = 0; t < c->step_T[i]; ++t) s.snap_slot[t] = c->step_snap[i][t];
-    if (out_counts) out_counts[i] = cnt;
-    for (int k = 0; k < cnt; ++k) {
-      if (out_tokens) out_tokens[at] = h[kOutTokens + at];
-      ++at;
-    }
-  }
+  if (!finish_seqs(c, h, out_tokens, out_counts)) return MK_ERR_CUDA;
   return nonfinite ? MK_ERR_NONFINITE : MK_OK;
 }
 
@@ -1077,20 +1106,7 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
       cudaStreamSynchronize(c->stream) != cudaSuccess)
     return MK_ERR_CUDA;
   if (h[kOutInts] != DEV_OK) return MK_ERR_BARRIER_TIMEOUT;
-  int at = 0;
-  for (int i = 0; i < c->n_seq; ++i) {
-    const int cnt = h[kOutCounts + i];
-    if (cnt < 1 || cnt > c->step_T[i]) return MK_ERR_CUDA;
-    SeqInfo& sq = c->seqs[c->step_seq[i]];
-    sq.pending = true;
-    sq.count = cnt;
-    for (int t = 0; t < c->step_T[i]; ++t) sq.snap_slot[t] = c->step_snap[i][t];
-    if (out_counts) out_counts[i] = cnt;
-    for (int k = 0; k < cnt; ++k) {
-      if (out_tokens) out_tokens[at] = h[kOutTokens + at];
-      ++at;
-    }
-  }
+  if (!finish_seqs(c, h, out_tokens, out_counts)) return MK_ERR_CUDA;
   return h[kOutInts + 1] ? MK_ERR_NONFINITE : MK_OK;
 }
 

@@ -168,6 +168,8 @@ struct StepDesc {
   int32_t row_tok[kMaxRows], row_pos[kMaxRows], row_si[kMaxRows];
   int32_t seq_id[kMaxSeqs], seq_row0[kMaxSeqs], seq_T[kMaxSeqs], seq_len[kMaxSeqs];
   int32_t seq_slot_in[kMaxSeqs], seq_snap_all[kMaxSeqs];
+  // 0: verify rows; 1: prompt rows; 2: prompt rows ending the prompt (one token)
+  int32_t seq_prompt[kMaxSeqs];
   int32_t seq_slot_out[kMaxSeqs][kMaxT];
   int32_t seq_nsplit[kMaxSeqs], seq_chunks_per_split[kMaxSeqs], seq_item0[kMaxSeqs];
   // attention plan of this step (attn_plan): warp groups and KV staging slots

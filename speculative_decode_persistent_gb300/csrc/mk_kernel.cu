@@ -1975,7 +1975,9 @@ __device__ __noinline__ void lm_argmax(const ModelDesc& md, const StepDesc& sd, 
 // ------------------------------------------------------------------ verify
 // Block 0: argmax of every row over all warps' top-2 records (lowest index on
 // exact ties), then per sequence the longest prefix of drafts that equal the
-// previous row's argmax; emitted = accepted drafts + the bonus argmax.
+// previous row's argmax; emitted = accepted drafts + the bonus argmax. A
+// sequence of prompt rows emits nothing, or the argmax of its last row when
+// the rows end its prompt.
 __device__ void verify_phase(const ModelDesc& md, const StepDesc& sd, const Smem& sm) {
   if (blockIdx.x != 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -2002,6 +2004,12 @@ __device__ void verify_phase(const ModelDesc& md, const StepDesc& sd, const Smem
     int at = 0;
     for (int si = 0; si < sd.n_seq; ++si) {
       const int T = sd.seq_T[si], row0 = sd.seq_row0[si];
+      if (sd.seq_prompt[si]) {  // prompt rows: no verification; one token when the prompt ends
+        const int emits = sd.seq_prompt[si] == 2 ? 1 : 0;
+        if (emits) md.out[kOutTokens + at++] = am[row0 + T - 1];
+        md.out[kOutCounts + si] = emits;
+        continue;
+      }
       int a = 0;
       while (a + 1 < T && sd.row_tok[row0 + a + 1] == am[row0 + a]) ++a;
       for (int i = 1; i <= a; ++i) md.out[kOutTokens + at++] = sd.row_tok[row0 + i];

@@ -54,16 +54,18 @@ class Pair:
         self.hidden = torch.zeros((12, H), dtype=torch.float32, device="cuda")
         self.eng.debug_outputs(self.logits, self.hidden)
 
-    def step(self, tokens, positions, seq_ids):
-        ro = self.oracle.step(tokens, positions, seq_ids, want_logits=True, want_hidden=True)
-        gt, gc = self.eng.step(tokens, positions, seq_ids)
+    def step(self, tokens, positions, seq_ids, flags=None):
+        ro = self.oracle.step(tokens, positions, seq_ids, flags=flags, want_logits=True, want_hidden=True)
+        gt, gc = self.eng.step(tokens, positions, seq_ids, flags=flags)
         R = len(tokens)
         gl = self.logits[:R].double().cpu().numpy()
         gh = self.hidden[:R].double().cpu().numpy()
         return ro, dict(tokens=gt, counts=gc, logits=gl, hidden=gh)
 
-    def compare_step(self, ro, rg, seq_ids):
-        """Returns (n_excused_rows, report dict); asserts the parity bar."""
+    def compare_step(self, ro, rg, seq_ids, flags=None):
+        """Returns (n_excused_rows, report dict); asserts the parity bar.
+        flags: the step's row flags (prompt rows emit at most the argmax of the
+        sequence's last row, so only a near-tie there is excused)."""
         R = len(seq_ids)
         rep = dict(max_logit_err_over_rms=0.0, hidden_rel_l2=0.0)
         for r in range(R):
@@ -87,6 +89,9 @@ class Pair:
             co, cg = int(ro["counts"][i]), int(rg["counts"][i])
             tie_rows = [j for j in range(T) if ro["gap"][row + j] < TIE_GAP * ro["rms"][row + j]]
             first_tie = min(tie_rows) if tie_rows else T
+            prompt = flags is not None and int(flags[row]) != 0
+            if prompt:
+                first_tie = 0 if (T - 1) in tie_rows else T
             if first_tie < co:  # the verify outcome may legitimately differ
                 excused += T - first_tie
             else:

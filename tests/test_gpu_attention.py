@@ -43,3 +43,20 @@ def test_attention_27b_heads(cuda_ok, kv_q8, case):
     p.compare_step(ro, rg, sid)
     for s in range(len(seqs)):
         p.compare_kv(s, [int(x) for x, q in zip(pos, sid) if q == s])
+
+
+@pytest.mark.parametrize("kv_q8", [0, 1])
+def test_attention_27b_heads_prompt_rows(cuda_ok, kv_q8):
+    """Eight prompt rows ending the prompt (flags 1 x 7, then 2) over a
+    2,000-token cache: causal over the rows, no verification, one token."""
+    seqs = [(2000, 8)]
+    ov = dict(model=_model(), kv_q8=kv_q8, n_pages=(2000 + 8 + 15) // 16 + 8, seqs=seqs)
+    p = Pair("qwen27-t1-4k-fp16", overrides=ov, nthreads=8)
+    tok = np.array(np.random.default_rng(13).integers(0, p.wl.model["vocab"], 8), np.int32)
+    pos = np.arange(2000, 2008, dtype=np.int32)
+    sid = np.zeros(8, np.int32)
+    flags = np.array([1] * 7 + [2], np.uint8)
+    ro, rg = p.step(tok, pos, sid, flags)
+    p.compare_step(ro, rg, sid, flags)
+    assert list(rg["counts"]) == [1]
+    p.compare_kv(0, pos.tolist())
