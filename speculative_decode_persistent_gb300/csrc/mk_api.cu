@@ -149,23 +149,6 @@ Plan make_plan(const mk_layout& L) {
   return p;
 }
 
-int max_segments(int n_tiles, int nsb, int grid) {
-  int best = 1;
-  for (int R = 1; R <= kMaxRows; ++R) {
-    const Sched sc = make_sched(nsb, R);
-    for (int sl = 0; sl < sc.S; ++sl) {
-      const int nsb_s = slice_nsb(sc, nsb, sl);
-      const uint32_t Us = static_cast<uint32_t>(n_tiles) * nsb_s;
-      const uint32_t Ws = static_cast<uint32_t>(slice_cta0(sc, grid, sl + 1) - slice_cta0(sc, grid, sl)) * kWarps;
-      for (uint32_t ws = 0; ws < Ws; ++ws) {
-        const uint32_t u0 = warp_u0(Us, Ws, ws), u1 = warp_u0(Us, Ws, ws + 1);
-        if (u1 > u0) best = std::max(best, static_cast<int>((u1 - 1) / nsb_s - u0 / nsb_s + 1));
-      }
-    }
-  }
-  return best;
-}
-
 struct SeqInfo {
   bool used = false;
   int len = 0;
@@ -392,7 +375,6 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   c->plan = make_plan(L);
   const Plan& p = c->plan;
   uint8_t* packed = static_cast<uint8_t*>(b->packed);
-  cudaError_t e = cudaSuccess;
   const int H = L.hidden, F = L.ffn;
 
   // ---- repack weights
@@ -510,16 +492,12 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   md.kv_q8 = L.kv_dtype == MK_KV_Q8; md.page_tokens = L.page_tokens; md.n_pages = L.n_pages;
   md.max_pages_per_seq = L.max_pages_per_seq; md.n_slots = L.n_state_slots; md.max_seqs = L.max_seqs;
   md.grid = c->grid; md.eps = L.rms_eps;
-  int gi = 0, fi = 0, max_tiles = 1, max_seg = 1;
+  int gi = 0, fi = 0, max_tiles = 1;
   auto gemm = [&](GemmDesc& g, const PhasePlan& ph, int pro, int epi, const float* gain) {
     g.w = packed + ph.off; g.n_tiles = ph.n_tiles; g.nsb = ph.nsb; g.n_out = ph.n_out;
     g.pro = pro; g.epi = epi; g.gain = gain;
     g.zero_buf = ZERO_NONE;
-    g.img_in = (pro == PRO_RMS_X || pro == PRO_H) ? 1 : 0;
-    g.img_out = 0;
-    g.img_gain = nullptr;
     max_tiles = std::max(max_tiles, ph.n_tiles);
-    max_seg = std::max(max_seg, max_segments(ph.n_tiles, ph.nsb, c->grid));
   };
   for (int l = 0; l < L.n_layers; ++l) {
     LayerDesc& ld = md.layer[l];
@@ -568,20 +546,8 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
     md.layer[l].o.zero_buf = ZERO_GU;
     md.layer[l].down.zero_buf = ZERO_YIN;
   }
-  // image producers: o_proj -> gate/up (ffn norm), gate/up -> down (no norm),
-  // down -> next layer's input projections (attention norm) or lm_head
-  for (int l = 0; l < L.n_layers; ++l) {
-    LayerDesc& ld = md.layer[l];
-    ld.o.img_out = 1;
-    ld.o.img_gain = ld.gu.gain;
-    ld.gu.img_out = 1;
-    ld.gu.img_gain = nullptr;
-    ld.down.img_out = 1;
-    ld.down.img_gain = l + 1 < L.n_layers ? md.layer[l + 1].in.gain : md.lm.gain;
-  }
   md.final_norm = reinterpret_cast<const float*>(packed + p.off_final_norm);
   md.embed = packed + p.off_embed;
-  md.max_seg = max_seg;
   md.kv_k = b->kv_k; md.kv_v = b->kv_v;
   md.kv_ks = static_cast<uint16_t*>(b->kv_k_scale); md.kv_vs = static_cast<uint16_t*>(b->kv_v_scale);
   const int n_kv = n_kv_of(&L);
@@ -595,34 +561,29 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   const size_t attn_items_max = static_cast<size_t>(2 * c->grid + kMaxSeqs * std::max(1, L.fa_hkv));
   c->tickets_bytes = static_cast<size_t>(max_tiles) * 4;
   c->attn_tickets_bytes = static_cast<size_t>(kMaxSeqs) * std::max(1, L.fa_hkv) * 4;
-  md.img_k = std::max(H, F);
-  if ((e = dev_alloc(c, &md.img_h[0], static_cast<size_t>(2 * kMaxRows) * md.img_k * 2)) ||
-      (e = dev_alloc(c, &md.img_h[1], static_cast<size_t>(2 * kMaxRows) * md.img_k * 2)) ||
-      (e = dev_alloc(c, &md.img_p[0], static_cast<size_t>(md.img_k / 16) * kMaxRows * 4)) ||
-      (e = dev_alloc(c, &md.img_p[1], static_cast<size_t>(md.img_k / 16) * kMaxRows * 4)) ||
-      (e = dev_alloc(c, &md.x, static_cast<size_t>(kMaxRows) * H * 4)) ||
-      (e = dev_alloc(c, &md.yin, static_cast<size_t>(kMaxRows) * p.n_in_max * 4)) ||
-      (e = dev_alloc(c, &md.o, static_cast<size_t>(kMaxRows) * std::max(1, p.o_stride) * 4)) ||
-      (e = dev_alloc(c, &md.h, static_cast<size_t>(kMaxRows) * F * 4)) ||
-      (e = dev_alloc(c, &md.gu, static_cast<size_t>(kMaxRows) * 2 * F * 4)) ||
-      (e = dev_alloc(c, &md.logits, static_cast<size_t>(kMaxRows) * L.vocab * 4)) ||
-      (e = dev_alloc(c, &md.tickets, c->tickets_bytes)) ||
-      (e = dev_alloc(c, &md.attn_part, attn_items_max * kMaxQRows * kPartStride * 4)) ||
-      (e = dev_alloc(c, &md.attn_tickets, c->attn_tickets_bytes)) ||
-      (e = dev_alloc(c, &md.top_val, nrec * kMaxRows * 4)) ||
-      (e = dev_alloc(c, &md.top_idx, nrec * kMaxRows * 4)) ||
-      (e = dev_alloc(c, &md.page_table, static_cast<size_t>(L.max_seqs) * L.max_pages_per_seq * 4)) ||
-      (e = dev_alloc(c, &md.out, kOutInts * 4)) ||
-      (e = dev_alloc(c, &md.bar, 64)) ||
-      (e = dev_alloc(c, &md.err, 64)) ||
-      (e = dev_alloc(c, &c->attn_scratch, nrec * 2 * kMaxDh * 4)) ||
-      (e = dev_alloc(c, &md.mtp_in, L.has_mtp ? static_cast<size_t>(kMaxRows) * 2 * H * 4 : 0)) ||
-      (e = dev_alloc(c, &md.mtp_h, L.has_mtp ? static_cast<size_t>(kMaxSeqs) * H * 4 : 0)) ||
-      (e = dev_alloc(c, &md.mtp_rope, static_cast<size_t>(kMaxSeqs) * (kMaxDh / 2) * sizeof(float2))) ||
-      (e = dev_alloc(c, &md.mtp_row, static_cast<size_t>(kMaxSeqs) * 2 * 4)) ||
-      (e = dev_alloc(c, &c->inv_freq, (kMaxDh / 2) * sizeof(double))) ||
-      (e = dev_alloc(c, &c->md_dev, sizeof(ModelDesc))) ||
-      (e = dev_alloc(c, &c->sd_dev, sizeof(StepDesc)))) {
+  if ((dev_alloc(c, &md.x, static_cast<size_t>(kMaxRows) * H * 4)) ||
+      (dev_alloc(c, &md.yin, static_cast<size_t>(kMaxRows) * p.n_in_max * 4)) ||
+      (dev_alloc(c, &md.o, static_cast<size_t>(kMaxRows) * std::max(1, p.o_stride) * 4)) ||
+      (dev_alloc(c, &md.h, static_cast<size_t>(kMaxRows) * F * 4)) ||
+      (dev_alloc(c, &md.gu, static_cast<size_t>(kMaxRows) * 2 * F * 4)) ||
+      (dev_alloc(c, &md.logits, static_cast<size_t>(kMaxRows) * L.vocab * 4)) ||
+      (dev_alloc(c, &md.tickets, c->tickets_bytes)) ||
+      (dev_alloc(c, &md.attn_part, attn_items_max * kMaxQRows * kPartStride * 4)) ||
+      (dev_alloc(c, &md.attn_tickets, c->attn_tickets_bytes)) ||
+      (dev_alloc(c, &md.top_val, nrec * kMaxRows * 4)) ||
+      (dev_alloc(c, &md.top_idx, nrec * kMaxRows * 4)) ||
+      (dev_alloc(c, &md.page_table, static_cast<size_t>(L.max_seqs) * L.max_pages_per_seq * 4)) ||
+      (dev_alloc(c, &md.out, kOutInts * 4)) ||
+      (dev_alloc(c, &md.bar, 64)) ||
+      (dev_alloc(c, &md.err, 64)) ||
+      (dev_alloc(c, &c->attn_scratch, nrec * 2 * kMaxDh * 4)) ||
+      (dev_alloc(c, &md.mtp_in, L.has_mtp ? static_cast<size_t>(kMaxRows) * 2 * H * 4 : 0)) ||
+      (dev_alloc(c, &md.mtp_h, L.has_mtp ? static_cast<size_t>(kMaxSeqs) * H * 4 : 0)) ||
+      (dev_alloc(c, &md.mtp_rope, static_cast<size_t>(kMaxSeqs) * (kMaxDh / 2) * sizeof(float2))) ||
+      (dev_alloc(c, &md.mtp_row, static_cast<size_t>(kMaxSeqs) * 2 * 4)) ||
+      (dev_alloc(c, &c->inv_freq, (kMaxDh / 2) * sizeof(double))) ||
+      (dev_alloc(c, &c->md_dev, sizeof(ModelDesc))) ||
+      (dev_alloc(c, &c->sd_dev, sizeof(StepDesc)))) {
     mk_free(c);
     return MK_ERR_CUDA;
   }
@@ -1009,7 +970,7 @@ constexpr int kMaxDevices = 64;
 void* g_static_addr[kMaxDevices] = {nullptr};
 
 struct StaticLayout {
-  size_t md, img_h0, img_h1, img_p0, img_p1, x, yin, o, h, gu, logits, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
+  size_t md, x, yin, o, h, gu, logits, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
       attn_scratch, total;
 };
 
@@ -1020,10 +981,6 @@ StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
   size_t at = 0;
   auto take = [&](size_t& off, size_t bytes) { off = at; at = align_up(at + (bytes ? bytes : 16)); };
   take(L.md, sizeof(ModelDesc));
-  take(L.img_h0, static_cast<size_t>(2 * kMaxRows) * md.img_k * 2);
-  take(L.img_h1, static_cast<size_t>(2 * kMaxRows) * md.img_k * 2);
-  take(L.img_p0, static_cast<size_t>(md.img_k / 16) * kMaxRows * 4);
-  take(L.img_p1, static_cast<size_t>(md.img_k / 16) * kMaxRows * 4);
   take(L.x, static_cast<size_t>(kMaxRows) * md.H * 4);
   take(L.yin, static_cast<size_t>(kMaxRows) * md.n_in_max * 4);
   take(L.o, static_cast<size_t>(kMaxRows) * std::max(1, md.o_stride) * 4);
@@ -1067,10 +1024,6 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
   const StaticLayout SL = static_layout(c, c->sd_host->n_attn_items);
   uint8_t* base = static_cast<uint8_t*>(g_static_addr[dev]);
   ModelDesc md = c->md_host;
-  md.img_h[0] = reinterpret_cast<__half*>(base + SL.img_h0);
-  md.img_h[1] = reinterpret_cast<__half*>(base + SL.img_h1);
-  md.img_p[0] = reinterpret_cast<float*>(base + SL.img_p0);
-  md.img_p[1] = reinterpret_cast<float*>(base + SL.img_p1);
   md.x = reinterpret_cast<float*>(base + SL.x);
   md.yin = reinterpret_cast<float*>(base + SL.yin);
   md.o = reinterpret_cast<float*>(base + SL.o);

@@ -81,11 +81,8 @@ enum Epilogue : int32_t { EPI_STORE_YIN = 0, EPI_RESID_X = 1, EPI_STORE_GU = 2, 
 struct GemmDesc {
   const uint8_t* w;  // units [n_tiles][nsb]
   int32_t n_tiles, nsb, n_out, pro, epi;
-  int32_t img_in;    // 1: the activations come from the image the previous phase wrote
-  int32_t img_out;   // 1: the epilogue writes the next phase's activation image
   int32_t dump;      // EPI_TOP2: 1 = copy the logits to the debug buffer (main lm_head)
-  const float* gain;      // RMSNorm gain (PRO_RMS_X) or per-head output-norm gain (PRO_GDN_OUT)
-  const float* img_gain;  // gain the written image is multiplied by (NULL: none)
+  const float* gain;  // RMSNorm gain (PRO_RMS_X) or per-head output-norm gain (PRO_GDN_OUT)
   // a buffer a later phase accumulates into, cleared (rows < R) at this phase's start
   int32_t zero_buf;  // ZERO_NONE, ZERO_GU or ZERO_YIN
   int32_t pad2;
@@ -103,7 +100,6 @@ struct ModelDesc {
   int32_t n_gdn, n_fa, n_in_max;      // y_in row stride
   int32_t o_stride;                   // o row stride
   int32_t kv_q8, page_tokens, n_pages, max_pages_per_seq, n_slots, max_seqs;
-  int32_t max_seg;                    // partial slots per warp per phase
   int32_t grid;                       // blocks of the persistent launch
   float eps;
   // layer[n_layers] is the MTP block when has_mtp
@@ -125,22 +121,12 @@ struct ModelDesc {
   void* kv_k; void* kv_v; uint16_t* kv_ks; uint16_t* kv_vs;
   float* gdn_state; float* conv_state;
   // scratch
-  // Activation images, double-buffered by phase parity: the phase that
-  // produces a GEMM's input writes it once, already split into fp16 high/low
-  // columns in the permuted B-fragment order (img_h [2*kMaxRows][img_k]) with
-  // per-16 sums of (high+low) (img_p [img_k/16][R]); RMSNorm's 1/rms is left
-  // out and applied to the GEMM's output rows instead.
-  __half* img_h[2];
-  float* img_p[2];
-  int32_t img_k;
-  int32_t pad_img;
   float* x;          // [kMaxRows][H] residual stream
   float* yin;        // [kMaxRows][n_in_max] input projections
   float* o;          // [kMaxRows][o_stride] mixer outputs
   float* h;          // [kMaxRows][F] SwiGLU output (written only while debug outputs are on)
   float* gu;         // [kMaxRows][2F] gate/up outputs, 16-row blocks of 8 gate + 8 up rows
   float* logits;     // [kMaxRows][V] lm_head outputs of split tiles (summed by red.add)s
-  float* partial;    // [grid*kWarps][max_seg][kMaxRows][32]
   uint32_t* tickets; // per tile
   float* attn_part;  // [attn items][kMaxQRows][kPartStride]: dims, then m and l (log2 units)
   uint32_t* attn_tickets;  // per (step sequence, kv head)
