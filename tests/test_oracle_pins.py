@@ -392,3 +392,28 @@ def test_prefill_rows_commit_and_emit():
     assert r["counts"].tolist() == [1]
     assert r["tokens"].tolist() == [int(r["argmax"][1])]
     assert o.seq_get(0)["length"] == 22
+
+
+def test_prompt_rows_invariant_to_chunking_and_batching():
+    """Prompt rows (the page's chunked prefill riding along with decode rows)
+    give the same committed state and emitted token whether the prompt comes
+    as one 8-row step, as two 4-row steps, or beside another sequence's
+    verify rows: rows of different sequences never interact, and the
+    recurrence runs row by row."""
+    prompt = [5, 77, 901, 13, 1500, 2, 640, 333]
+    flags = [1] * 7 + [2]
+    wl, one = _tiny_oracle(seqs=[(64, 4), (16, 8)], n_pages=32)
+    r1 = one.step(prompt, list(range(16, 24)), [1] * 8, flags=flags)
+    wl, two = _tiny_oracle(seqs=[(64, 4), (16, 8)], n_pages=32)
+    two.step(prompt[:4], list(range(16, 20)), [1] * 4, flags=[1] * 4)
+    r2 = two.step(prompt[4:], list(range(20, 24)), [1] * 4, flags=[1, 1, 1, 2])
+    wl, mixed = _tiny_oracle(seqs=[(64, 4), (16, 8)], n_pages=32)
+    r3 = mixed.step([1, 2, 3, 4] + prompt, list(range(64, 68)) + list(range(16, 24)), [0] * 4 + [1] * 8,
+                    flags=[0] * 4 + flags)
+    assert r1["tokens"].tolist() == r2["tokens"].tolist() == [int(r3["tokens"][-1])]
+    s1, s2, s3 = one.seq_get(1), two.seq_get(1), mixed.seq_get(1)
+    assert s1["length"] == s2["length"] == s3["length"] == 24
+    for k in ("S", "conv"):
+        assert np.max(np.abs(s1[k] - s2[k])) <= 1e-12 * np.max(np.abs(s1[k]))
+        assert np.array_equal(s1[k], s3[k])
+    assert np.max(np.abs(r1["logits"][7] - r2["logits"][3])) <= 1e-12 * np.max(np.abs(r1["logits"][7]))
