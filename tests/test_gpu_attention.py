@@ -60,3 +60,17 @@ def test_attention_27b_heads_prompt_rows(cuda_ok, kv_q8):
     p.compare_step(ro, rg, sid, flags)
     assert list(rg["counts"]) == [1]
     p.compare_kv(0, pos.tolist())
+
+
+def test_attention_27b_heads_96k_q8(cuda_ok):
+    """The long-context workload's attention at full size: T = 5 rows over a
+    96,000-token q8 cache (about 38 splits of 158 pages per kv head, merged by
+    all of a head's split blocks), against the oracle."""
+    seqs = [(96000, 5)]
+    ov = dict(model=_model(), kv_q8=1, n_pages=(96000 + 5 + 15) // 16 + 8, seqs=seqs)
+    p = Pair("qwen27-t1-4k-fp16", overrides=ov, nthreads=16)
+    rng = np.random.default_rng(17)
+    tok, pos, sid = p.wl.rows([list(rng.integers(0, p.wl.model["vocab"], 4))])
+    ro, rg = p.step(tok, pos, sid)
+    p.compare_step(ro, rg, sid)
+    p.compare_kv(0, [int(x) for x in pos])
