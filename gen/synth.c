@@ -17,9 +17,14 @@
  * constants of Vigna's reference code). The n-th output of a SplitMix64
  * stream seeded with s is mix64(s + (n+1)*0x9E3779B97F4A7C15).
  *
- * Normal deviates: Irwin-Hall with four terms. The four 16-bit fields of one
- * 64-bit draw are summed and standardised, z = (sum - 131070) * sqrt(3)/65536,
- * which has mean 0 and variance 1 (bounded at +-3.46).
+ * Normal deviates: the Box-Muller transform (Box and Muller, "A note on the
+ * generation of random normal deviates", Ann. Math. Statist. 1958): the two
+ * 32-bit halves of one 64-bit draw give u1, u2 in (0, 1) and
+ * z = sqrt(-2 ln u1) cos(2 pi u2), a standard normal deviate (tails to about
+ * 6.8 sigma). ln and cos are evaluated here by fixed series in plain IEEE
+ * double arithmetic, not by the C library, so every platform produces the
+ * same bits: ln(m 2^e) = e ln 2 + 2 atanh((m-1)/(m+1)) for m in [1, 2), and
+ * cos by its Taylor series after reducing the angle to [-pi, pi].
  */
 #include <math.h>
 #include <stdint.h>
@@ -45,12 +50,42 @@ static inline uint64_t draw(uint64_t base, uint64_t idx) {
     return mix64(base + (idx + 1) * GOLDEN);
 }
 
-static const double IH_SCALE = 1.7320508075688772 / 65536.0; /* sqrt(3)/2^16 */
+static const double LN2 = 0.69314718055994530942;
+static const double TWO_PI = 6.28318530717958647692;
+static const double PI_ = 3.14159265358979323846;
+
+/* ln x for x in (0, 1]: x = m 2^e with m in [1, 2) (exact, frexp), then
+ * ln m = 2 atanh(s), s = (m-1)/(m+1) <= 1/3, summed to s^41. */
+static double ln_series(double x) {
+    int e;
+    double m = frexp(x, &e); /* x = m 2^e, m in [0.5, 1) */
+    m *= 2.0;
+    e -= 1;
+    const double t = (m - 1.0) / (m + 1.0), t2 = t * t;
+    double term = t, sum = 0.0;
+    for (int k = 1; k <= 41; k += 2) {
+        sum += term / (double)k;
+        term *= t2;
+    }
+    return (double)e * LN2 + 2.0 * sum;
+}
+
+/* cos a for a in [0, 2 pi): reduced to [-pi, pi], Taylor series to a^40. */
+static double cos_series(double a) {
+    if (a > PI_) a -= TWO_PI;
+    const double a2 = a * a;
+    double term = 1.0, sum = 1.0;
+    for (int n = 1; n <= 20; ++n) {
+        term *= -a2 / (double)((2 * n - 1) * (2 * n));
+        sum += term;
+    }
+    return sum;
+}
 
 static inline double normal_from(uint64_t h) {
-    int64_t s = (int64_t)(h & 0xFFFF) + (int64_t)((h >> 16) & 0xFFFF) +
-                (int64_t)((h >> 32) & 0xFFFF) + (int64_t)((h >> 48) & 0xFFFF);
-    return (double)(s - 131070) * IH_SCALE;
+    const double u1 = ((double)(h >> 32) + 0.5) * (1.0 / 4294967296.0);
+    const double u2 = ((double)(h & 0xFFFFFFFFu) + 0.5) * (1.0 / 4294967296.0);
+    return sqrt(-2.0 * ln_series(u1)) * cos_series(TWO_PI * u2);
 }
 
 /* Uniform double in [0, 1) with 53 random bits. */

@@ -161,6 +161,11 @@ size_t mk_gdn_state_bytes(const mk_layout* layout); /* whole gdn_state buffer */
 size_t mk_conv_state_bytes(const mk_layout* layout);/* whole conv_state buffer */
 
 /*
+ * Passage: page "OpenJet's CUDA megakernel runs 4 coding agents on one RTX
+ * 3090", section "Why it matters" (every step reads all the weights once and
+ * stacks every active sequence's rows onto that one read), for the model of
+ * page "Fusing the whole speculative-decoding cycle into one CUDA kernel",
+ * section "What shipped" (64 layers: 48 Gated DeltaNet, 16 gated attention).
  * Create a context: validates the layout, repacks the canonical weights into
  * buffers->packed (tile order for streaming; the canonical tensors may be
  * freed afterwards), and allocates scratch. stream is a cudaStream_t (NULL =
@@ -171,7 +176,10 @@ size_t mk_conv_state_bytes(const mk_layout* layout);/* whole conv_state buffer *
 mk_status mk_create(const mk_layout* layout, const mk_weights* weights,
                     const mk_buffers* buffers, void* stream, mk_ctx** out);
 
-/* Release the context, its scratch and pinned buffers. Borrowed buffers are
+/* The end of a context made by mk_create (the pages describe the engine's
+ * step, not its teardown: page "Fusing the whole speculative-decoding cycle
+ * into one CUDA kernel", section "What shipped").
+ * Release the context, its scratch and pinned buffers. Borrowed buffers are
  * untouched. NULL is accepted. */
 void mk_free(mk_ctx* ctx);
 
@@ -194,6 +202,12 @@ mk_status mk_seq_get(mk_ctx* ctx, int32_t seq, int32_t* length, int32_t* pages,
                      int32_t* n_pages, int32_t* state_slot);
 
 /*
+ * Passage: page "Fusing the whole speculative-decoding cycle into one CUDA
+ * kernel", section "What shipped" (one persistent cooperative launch runs
+ * the main model over T = 1 + n_draft rows, lm_head and verification on the
+ * device), and page "OpenJet's CUDA megakernel runs 4 coding agents on one
+ * RTX 3090", section "Why it matters" (all agents' rows in one batch per
+ * step, the host reading back only the accepted tokens).
  * One verify step, synchronous on the context's stream.
  * Rows (host arrays of n_rows): rows of one sequence are contiguous, have
  * consecutive positions starting at the sequence's committed length, and
@@ -253,6 +267,9 @@ mk_status mk_step_finish(mk_ctx* ctx, int32_t* out_tokens, int32_t* out_counts);
 mk_status mk_last_drafts(mk_ctx* ctx, int32_t* drafts);
 
 /*
+ * Passage: page "Fusing the whole speculative-decoding cycle into one CUDA
+ * kernel", section "What shipped", the model paragraph (the recurrent state
+ * is committed only through the surely-accepted token).
  * Keep n_keep[i] rows (1 <= n_keep[i] <= count of its last step) of each
  * pending sequence seq_ids[i]: the length grows by n_keep, the committed state
  * becomes the one after row n_keep-1, and pages wholly beyond the new length
@@ -303,24 +320,35 @@ mk_status mk_step_io_bytes(mk_ctx* ctx, uint64_t* h2d_bytes, uint64_t* d2h_bytes
 int32_t mk_grid_blocks(mk_ctx* ctx);
 
 /*
- * Allocation-free step (no counterpart on the pages: a deployment aid).
- * For callers that cannot allocate device memory when they step — code
- * running while a CUDA graph is being captured, or inside a memory pool or
- * allocator that must not grow — this runs the same step as mk_step with the
- * same arguments, results and bookkeeping, but every piece of per-step device
- * scratch the kernel writes comes from one file-scope device array of
- * 16 MiB that the library holds on each GPU where it is loaded, until the
- * process exits. The call makes no cudaMalloc, cudaFree or other allocating
- * call; the context itself must already exist (mk_create allocates).
+ * Allocation-free step. The pages have no counterpart of this entry point:
+ * it is a deployment aid.
+ * Some callers cannot allocate device memory at the moment they step: a
+ * server that reserved all of the GPU's memory up front for its own pool
+ * (a cudaMalloc there fails, or forces the pool to give memory back), an
+ * allocator that must not grow or fragment while requests are in flight,
+ * or a latency-critical loop in which a cudaMalloc/cudaFree, which can
+ * synchronise the whole device, would stall work on other streams. For
+ * them this runs the same step as mk_step, with the same arguments, results
+ * and bookkeeping, but every piece of per-step device scratch the kernel
+ * writes comes from one file-scope device array of 16 MiB that the library
+ * holds on each GPU where it is loaded, until the process exits. The call
+ * makes no cudaMalloc, cudaFree or other allocating call; the context itself
+ * must already exist (mk_create allocates). Like mk_step it returns after
+ * the results are on the host.
  *  - Sizes: a context whose worst-case step scratch exceeds 16 MiB is refused
  *    with MK_ERR_UNSUPPORTED before any bookkeeping changes (small models
  *    fit; the 27B-shaped model does not). So is a model with an MTP head.
+ *  - The device that is current must be the context's device
+ *    (MK_ERR_INVALID otherwise).
  *  - The first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress; make that first call before any stream capture.
  *  - Every call shares the one array and it keeps the previous call's
  *    contents: the call clears the counters that must start at zero itself.
  *    Calls whose work overlaps on the GPU (two contexts or two streams at
  *    once) race on the array and give wrong results; serialise them.
+ *  - mk_last_launch_ms and mk_step_io_bytes report this call as they do
+ *    mk_step; mk_debug_scratch reads the context's own buffers, which this
+ *    call does not write.
  */
 mk_status mk_step_static(mk_ctx* ctx, int32_t n_rows, const int32_t* tokens, const int32_t* positions,
                          const int32_t* seq_ids, const uint8_t* row_flags, int32_t* out_tokens,

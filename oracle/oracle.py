@@ -61,42 +61,65 @@ class OrcPool(ctypes.Structure):
 _lib = None
 
 
+def _bind(L):
+    L.orc_create.restype = vp
+    L.orc_create.argtypes = [ctypes.POINTER(OrcLayout), ctypes.POINTER(OrcWeights),
+                             ctypes.POINTER(OrcPool), i32]
+    L.orc_free.argtypes = [vp]
+    L.orc_seq_set.argtypes = [vp, i32, i32, vp, i32, vp, vp]
+    L.orc_seq_get.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+    L.orc_commit.argtypes = [vp, i32, vp, vp]
+    L.orc_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.orc_drafts.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+    L.orc_q4_decode.argtypes = [vp, i64, vp]
+    L.orc_q4_encode.argtypes = [vp, i64, vp]
+    L.orc_q4_matvec.argtypes = [vp, i32, i32, vp, vp, i32]
+    L.orc_q8_encode.argtypes = [vp, i64, vp, vp]
+    L.orc_half_round.argtypes = [dbl]
+    L.orc_half_round.restype = ctypes.c_uint16
+    L.orc_half_value.argtypes = [ctypes.c_uint16]
+    L.orc_half_value.restype = dbl
+    L.orc_rmsnorm.argtypes = [vp, vp, i32, dbl, vp]
+    L.orc_l2norm.argtypes = [vp, i32, dbl]
+    L.orc_rope.argtypes = [vp, i32, i32, dbl]
+    L.orc_attend.argtypes = [vp, vp, vp, i32, i32, vp]
+    L.orc_gdn_update.argtypes = [vp, i32, i32, vp, vp, vp, dbl, dbl, vp]
+    L.orc_sigmoid.argtypes = [dbl]
+    L.orc_sigmoid.restype = dbl
+    L.orc_silu.argtypes = [dbl]
+    L.orc_silu.restype = dbl
+    L.orc_n_free_pages.argtypes = [vp]
+    for f in ("orc_seq_set", "orc_seq_get", "orc_commit", "orc_step", "orc_n_free_pages", "orc_drafts"):
+        getattr(L, f).restype = ctypes.c_int
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_SO)
-        L.orc_create.restype = vp
-        L.orc_create.argtypes = [ctypes.POINTER(OrcLayout), ctypes.POINTER(OrcWeights),
-                                 ctypes.POINTER(OrcPool), i32]
-        L.orc_free.argtypes = [vp]
-        L.orc_seq_set.argtypes = [vp, i32, i32, vp, i32, vp, vp]
-        L.orc_seq_get.argtypes = [vp, i32, vp, vp, vp, vp, vp]
-        L.orc_commit.argtypes = [vp, i32, vp, vp]
-        L.orc_step.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-        L.orc_drafts.argtypes = [vp, i32, vp, vp, vp, vp, vp]
-        L.orc_q4_decode.argtypes = [vp, i64, vp]
-        L.orc_q4_encode.argtypes = [vp, i64, vp]
-        L.orc_q4_matvec.argtypes = [vp, i32, i32, vp, vp, i32]
-        L.orc_q8_encode.argtypes = [vp, i64, vp, vp]
-        L.orc_half_round.argtypes = [dbl]
-        L.orc_half_round.restype = ctypes.c_uint16
-        L.orc_half_value.argtypes = [ctypes.c_uint16]
-        L.orc_half_value.restype = dbl
-        L.orc_rmsnorm.argtypes = [vp, vp, i32, dbl, vp]
-        L.orc_l2norm.argtypes = [vp, i32, dbl]
-        L.orc_rope.argtypes = [vp, i32, i32, dbl]
-        L.orc_attend.argtypes = [vp, vp, vp, i32, i32, vp]
-        L.orc_gdn_update.argtypes = [vp, i32, i32, vp, vp, vp, dbl, dbl, vp]
-        L.orc_sigmoid.argtypes = [dbl]
-        L.orc_sigmoid.restype = dbl
-        L.orc_silu.argtypes = [dbl]
-        L.orc_silu.restype = dbl
-        L.orc_n_free_pages.argtypes = [vp]
-        for f in ("orc_seq_set", "orc_seq_get", "orc_commit", "orc_step", "orc_n_free_pages", "orc_drafts"):
-            getattr(L, f).restype = ctypes.c_int
-        _lib = L
+        _lib = _bind(ctypes.CDLL(_SO))
     return _lib
+
+
+def build_variant(substitutions: list[tuple[str, str]], out_dir: str):
+    """A copy of the oracle with each (old, new) source substitution applied
+    (each `old` must occur exactly once), compiled into out_dir and loaded.
+    Tests use it to plant a known mistake and check that a pin catches it."""
+    with open(_SRC) as f:
+        src = f.read()
+    for old, new in substitutions:
+        n = src.count(old)
+        if n != 1:
+            raise ValueError(f"substitution target occurs {n} times: {old!r}")
+        src = src.replace(old, new)
+    os.makedirs(out_dir, exist_ok=True)
+    cpp = os.path.join(out_dir, "oracle_variant.cpp")
+    so = os.path.join(out_dir, "liboracle_variant.so")
+    with open(cpp, "w") as f:
+        f.write(src)
+    subprocess.check_call(["g++", *_FLAGS, "-o", so, cpp])
+    return _bind(ctypes.CDLL(so))
 
 
 def _p(a):
@@ -125,7 +148,8 @@ class Oracle:
     """fp64 CPU model step over numpy-held weights and a numpy-held KV pool."""
 
     def __init__(self, model: dict, weights: dict, pool: dict, kv_q8: int, n_pages: int,
-                 max_seqs: int, nthreads: int | None = None, n_draft: int = 0):
+                 max_seqs: int, nthreads: int | None = None, n_draft: int = 0, library=None):
+        self._lib = library if library is not None else lib()
         self.model = model
         self._keep = [weights, pool]
         self.L = make_layout(model, kv_q8, n_pages, max_seqs, n_draft=n_draft)
@@ -153,13 +177,13 @@ class Oracle:
                 setattr(P, n, _p(pool[n]))
         self.W, self.P = W, P
         self.nthreads = int(nthreads or os.cpu_count() or 1)
-        self.h = lib().orc_create(ctypes.byref(self.L), ctypes.byref(W), ctypes.byref(P), self.nthreads)
+        self.h = self._lib.orc_create(ctypes.byref(self.L), ctypes.byref(W), ctypes.byref(P), self.nthreads)
         if not self.h:
             raise ValueError("orc_create rejected the layout")
 
     def __del__(self):
         if getattr(self, "h", None):
-            lib().orc_free(self.h)
+            self._lib.orc_free(self.h)
             self.h = None
 
     # dims
@@ -176,7 +200,7 @@ class Oracle:
         pages = np.ascontiguousarray(pages, dtype=np.int32)
         S = None if S is None else np.ascontiguousarray(S, dtype=np.float32)
         conv = None if conv is None else np.ascontiguousarray(conv, dtype=np.float32)
-        rc = lib().orc_seq_set(self.h, seq, length, _p(pages), len(pages), _p(S), _p(conv))
+        rc = self._lib.orc_seq_set(self.h, seq, length, _p(pages), len(pages), _p(S), _p(conv))
         if rc:
             raise ValueError(f"orc_seq_set failed ({rc})")
 
@@ -186,7 +210,7 @@ class Oracle:
         pages = np.zeros(self.L.n_pages, np.int32)
         S = np.zeros((self.n_gdn, m["hv"], m["dv"], m["dk"]), np.float64)
         conv = np.zeros((self.n_gdn, m["conv_w"] - 1, self.conv_ch), np.float64)
-        rc = lib().orc_seq_get(self.h, seq, ctypes.byref(length), _p(pages), ctypes.byref(npg), _p(S), _p(conv))
+        rc = self._lib.orc_seq_get(self.h, seq, ctypes.byref(length), _p(pages), ctypes.byref(npg), _p(S), _p(conv))
         if rc:
             raise ValueError("orc_seq_get failed")
         return dict(length=length.value, pages=pages[: npg.value].copy(), S=S, conv=conv)
@@ -194,7 +218,7 @@ class Oracle:
     def commit(self, seq_ids, n_keep):
         s = np.ascontiguousarray(seq_ids, np.int32)
         k = np.ascontiguousarray(n_keep, np.int32)
-        rc = lib().orc_commit(self.h, len(s), _p(s), _p(k))
+        rc = self._lib.orc_commit(self.h, len(s), _p(s), _p(k))
         if rc:
             raise ValueError(f"orc_commit failed ({rc})")
 
@@ -212,7 +236,7 @@ class Oracle:
         argmax = np.zeros(R, np.int32)
         gap = np.zeros(R, np.float64)
         rms = np.zeros(R, np.float64)
-        rc = lib().orc_step(self.h, R, _p(tokens), _p(positions), _p(seq_ids), _p(fl),
+        rc = self._lib.orc_step(self.h, R, _p(tokens), _p(positions), _p(seq_ids), _p(fl),
                             _p(out_tokens), _p(out_counts), _p(logits), _p(hidden), _p(argmax),
                             _p(gap), _p(rms))
         if rc:
@@ -230,13 +254,13 @@ class Oracle:
         rms = np.zeros(n, np.float64)
         logits = np.zeros((n, m["draft_vocab"]), np.float64)
         hidden = np.zeros((n, m["hidden"]), np.float64)
-        rc = lib().orc_drafts(self.h, seq, _p(d), _p(gap), _p(rms), _p(logits), _p(hidden))
+        rc = self._lib.orc_drafts(self.h, seq, _p(d), _p(gap), _p(rms), _p(logits), _p(hidden))
         if rc:
             raise ValueError(f"orc_drafts failed ({rc})")
         return dict(tokens=d, gap=gap, rms=rms, logits=logits, hidden=hidden)
 
     def n_free_pages(self):
-        return lib().orc_n_free_pages(self.h)
+        return self._lib.orc_n_free_pages(self.h)
 
 
 # ------------------------------------------------------------------ blocks

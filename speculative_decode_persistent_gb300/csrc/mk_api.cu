@@ -166,6 +166,7 @@ struct mk_ctx {
   std::vector<int32_t> drafts;  // [sequences of the last completed step][n_draft]
   Plan plan;
   cudaStream_t stream = nullptr;
+  int device = 0;  // the device current at mk_create
   int grid = 0;
   ModelDesc md_host;
   ModelDesc* md_dev = nullptr;
@@ -237,20 +238,23 @@ cudaError_t upload_pages(mk_ctx* c, int seq) {
 // step commits); prompt rows are committed through their last row at once.
 // False when the device reported an impossible count.
 bool finish_seqs(mk_ctx* c, const int32_t* h, int32_t* out_tokens, int32_t* out_counts) {
+  // every count is checked before any sequence changes, so an impossible
+  // result block leaves the bookkeeping as it was
+  for (int i = 0; i < c->n_seq; ++i) {
+    const int cnt = h[kOutCounts + i];
+    if (c->step_prompt[i] ? cnt != (c->step_prompt[i] == 2 ? 1 : 0) : (cnt < 1 || cnt > c->step_T[i])) return false;
+  }
   int at = 0;
   for (int i = 0; i < c->n_seq; ++i) {
     const int cnt = h[kOutCounts + i];
     const int T = c->step_T[i];
     SeqInfo& s = c->seqs[c->step_seq[i]];
     for (int t = 0; t < T; ++t) s.snap_slot[t] = c->step_snap[i][t];
+    s.pending = true;
     if (c->step_prompt[i]) {
-      if (cnt != (c->step_prompt[i] == 2 ? 1 : 0)) return false;
-      s.pending = true;
       s.count = T;
       commit_seq(c, s, T);
     } else {
-      if (cnt < 1 || cnt > T) return false;
-      s.pending = true;
       s.count = cnt;
     }
     if (out_counts) out_counts[i] = cnt;
@@ -477,7 +481,8 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   int bps = 0;
   if (configure_persistent(&bps) != cudaSuccess || bps < 1) { mk_free(c); return MK_ERR_LAUNCH; }
   int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) { mk_free(c); return MK_ERR_CUDA; }
+  c->device = dev;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   c->grid = sms;  // one block per SM: the block owns the SM's shared memory
 
@@ -1013,6 +1018,8 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
   if (static_layout(c, worst_items).total > kStaticScratchBytes) return MK_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MK_ERR_CUDA;
+  // the array's address is per device: the context's device must be current
+  if (dev != c->device) return MK_ERR_INVALID;
   if (!g_static_addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_mk_static_scratch) != cudaSuccess || !p) return MK_ERR_CUDA;
@@ -1048,11 +1055,16 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
       cudaMemsetAsync(md.err, 0, 64, c->stream) != cudaSuccess ||
       cudaStreamSynchronize(c->stream) != cudaSuccess)
     return MK_ERR_CUDA;
+  c->h2d_bytes += sizeof(ModelDesc);
+  cudaEventRecord(c->ev0, c->stream);
   const cudaError_t e = launch_persistent(md_dev, c->sd_dev, attn_scratch, c->grid, &c->tm_k, &c->tm_v, c->stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? MK_ERR_LAUNCH : MK_ERR_CUDA;
   }
+  cudaEventRecord(c->ev1, c->stream);
+  c->timed = true;
+  c->d2h_bytes = kOutInts * 4 + 16;
   int32_t* h = c->out_host;
   if (cudaMemcpyAsync(h, md.out, kOutInts * 4, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||
       cudaMemcpyAsync(h + kOutInts, md.err, 16, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess ||

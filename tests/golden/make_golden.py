@@ -23,7 +23,20 @@ from gen.workload import Workload  # noqa: E402
 from oracle import oracle as orc  # noqa: E402
 
 OUT = os.path.join(HERE, "tiny_oracle_step.json")
-DRAFTS = [336, 1088, 7]  # the greedy continuation for two rows, then a wrong draft
+
+
+def greedy_drafts(wl, model):
+    """Drafts for the fixture step: the oracle's greedy continuation for two
+    rows (one-row passes), then a wrong token, so two drafts are accepted."""
+    o = orc.Oracle(wl.model, wl.weights, wl.pool, wl.kv_q8, wl.n_pages, wl.max_seqs, nthreads=2)
+    o.seq_set(0, wl.seqs[0][0], wl.tables[0], *wl.states[0])
+    tok, pos, out = int(wl.first_tokens[0]), wl.seqs[0][0], []
+    for j in range(2):
+        r = o.step([tok], [pos + j], [0], want_logits=False)
+        o.commit([0], [1])
+        tok = int(r["argmax"][0])
+        out.append(tok)
+    return out + [(out[-1] * 31 + 7) % model["vocab"]]
 
 
 def run(model, n_draft):
@@ -31,7 +44,7 @@ def run(model, n_draft):
     o = orc.Oracle(wl.model, wl.weights, wl.pool, wl.kv_q8, wl.n_pages, wl.max_seqs, nthreads=2,
                    n_draft=n_draft)
     o.seq_set(0, wl.seqs[0][0], wl.tables[0], *wl.states[0])
-    tok, pos, sid = wl.rows([DRAFTS])
+    tok, pos, sid = wl.rows([greedy_drafts(wl, model)])
     r = o.step(tok, pos, sid, want_hidden=True)
     out = dict(tokens=[int(t) for t in tok], positions=[int(p) for p in pos],
                emitted=[int(t) for t in r["tokens"]], counts=[int(c) for c in r["counts"]],

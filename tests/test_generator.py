@@ -39,13 +39,33 @@ def test_determinism_and_thread_independence():
 
 
 def test_normal_moments():
+    """Box-Muller deviates: mean 0, variance 1, the normal's kurtosis 3 (a
+    four-term Irwin-Hall sum would give 2.7 and never pass 3.47), tails past
+    4 sigma at about the normal rate, and the normal CDF at a few points."""
     z = gen.normal_f64(0, 9, 400000)
     assert abs(z.mean()) < 0.01
     assert abs(z.std() - 1.0) < 0.01
-    assert np.abs(z).max() <= 2 * np.sqrt(3) + 1e-12
-    # Irwin-Hall(4) kurtosis is 3 - 1.2/4 = 2.7
     k = np.mean(z ** 4)
-    assert abs(k - 2.7) < 0.05
+    assert abs(k - 3.0) < 0.05
+    assert np.abs(z).max() > 4.0
+    tail = np.mean(np.abs(z) > 3.0)  # 2 * (1 - Phi(3)) = 0.0026998
+    assert abs(tail - 0.0026998) < 0.0006
+    for x, phi in ((-1.0, 0.1586553), (0.5, 0.6914625), (2.0, 0.9772499)):
+        assert abs(np.mean(z <= x) - phi) < 0.003
+
+
+def test_normal_deviates_are_box_muller_of_the_draws():
+    """Each deviate is sqrt(-2 ln u1) cos(2 pi u2) of its own 64-bit draw
+    (u1, u2 from the high and low 32-bit halves), to within the error of the
+    generator's own ln/cos series."""
+    n = 2000
+    raw = gen.raw_draws(4, 21, n)
+    z = gen.normal_f64(4, 21, n)
+    hi = (raw >> np.uint64(32)).astype(np.float64)
+    lo = (raw & np.uint64(0xFFFFFFFF)).astype(np.float64)
+    u1, u2 = (hi + 0.5) / 2.0 ** 32, (lo + 0.5) / 2.0 ** 32
+    want = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+    assert np.max(np.abs(z - want)) < 1e-12
 
 
 def test_generator_q4_equals_oracle_quantiser():
