@@ -41,3 +41,53 @@ def test_mtp_passes_add_their_bytes():
         assert ab["kv"] - base["kv"] == n_draft * (4096 + 5) * 4 * 256 * 2 * 2
     # four passes: 1.33 GB, about 9 % of the step
     assert abs((ab["total"] - base["total"]) / 1e9 - 1.37) < 0.05
+
+
+class _FakeWl:
+    def __init__(self, seqs, vocab=100):
+        import numpy as np
+        self.seqs = seqs
+        self.model = {"vocab": vocab}
+        self.first_tokens = np.arange(7, 7 + len(seqs), dtype=np.int32)
+
+
+def test_drafter_follows_trajectory_with_seeded_mismatch():
+    """Each sequence's drafts copy its greedy trajectory up to the seeded
+    mismatch position m, then differ: a greedy verifier accepts exactly m;
+    advancing by the emitted count moves along the trajectory. Over many
+    steps m is uniform over 0..T-1."""
+    import numpy as np
+    b = _bench()
+    seqs = [(50, 3), (80, 3), (10, 3), (23, 3)]
+    wl = _FakeWl(seqs)
+    traj = [[(13 * s + 5 * j) % 100 for j in range(400)] for s in range(4)]
+    d = b.Drafter(wl, traj, 2)
+    seen = np.zeros(3, int)
+    for step in range(60):
+        tok, pos, sid = d.rows()
+        at = 0
+        out_t, out_c = [], []
+        for s, (cached, T) in enumerate(seqs):
+            rows = tok[at:at + T]
+            assert list(sid[at:at + T]) == [s] * T
+            assert list(pos[at:at + T]) == list(range(cached + d.off[s], cached + d.off[s] + T))
+            assert rows[0] == d.last[s]
+            o = d.off[s]
+            a = 0  # greedy acceptance against the trajectory
+            while a + 1 < T and rows[a + 1] == traj[s][o + a]:
+                a += 1
+            seen[a] += 1
+            out_t += [int(x) for x in rows[1:a + 1]] + [traj[s][o + a]]
+            out_c.append(a + 1)
+            at += T
+        before = list(d.off)
+        d.advance(np.array(out_t), np.array(out_c))
+        assert [d.off[s] - before[s] for s in range(4)] == out_c
+    assert seen.min() > 0.2 * seen.sum() / 3  # every accept length occurs
+
+
+def test_both_arms_share_the_config():
+    b = _bench()
+    a = b.workload_config("qwen27-4x3-23k-q8")
+    assert a == b.workload_config("qwen27-4x3-23k-q8")
+    assert a["rows_per_step"] == 12 and a["sequences"] == 4 and a["kv"] == "q8"
