@@ -57,6 +57,7 @@ def _reinstall(p):
         p.oracle.seq_set(s, cached, wl.tables[s], *wl.states[s])
         p.eng.seq_reset(s)
         p.eng.seq_set(s, cached, wl.tables[s], *wl.states[s])
+    p.reset_flips()
 
 
 @pytest.mark.parametrize("case", list(CASES))
