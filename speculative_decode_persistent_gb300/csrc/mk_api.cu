@@ -82,8 +82,13 @@ bool layout_ok(const mk_layout& L) {
   if (L.max_seqs <= 0 || L.max_seqs > MK_MAX_SEQS || L.max_pages_per_seq <= 0) return false;
   if (L.n_state_slots < 2) return false;
   if (!(L.rms_eps >= 0.f)) return false;
+  // an RMSNorm phase's reduction slices at the most rows must fit the row-sum slots
+  if (make_sched(L.hidden / 256, kMaxRows).S > kMaxNormSlices) return false;
   return true;
 }
+
+// GEMM phases of one launch: four per layer, lm_head, six per MTP draft pass.
+int gemm_phases(const mk_layout& L) { return 4 * L.n_layers + 1 + (L.has_mtp ? 6 * L.n_draft : 0); }
 
 Plan make_plan(const mk_layout& L) {
   Plan p;
@@ -565,7 +570,9 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   const size_t nrec = static_cast<size_t>(c->grid) * kWarps;
   const size_t attn_items_max = static_cast<size_t>(2 * c->grid + kMaxSeqs * std::max(1, L.fa_hkv));
   c->tickets_bytes = static_cast<size_t>(max_tiles) * 4;
-  c->attn_tickets_bytes = static_cast<size_t>(kMaxSeqs) * std::max(1, L.fa_hkv) * 4;
+  // the attention split counters, then the RMSNorm slice counters (one per GEMM phase)
+  const size_t attn_counters = static_cast<size_t>(kMaxSeqs) * std::max(1, L.fa_hkv);
+  c->attn_tickets_bytes = (attn_counters + gemm_phases(L)) * 4;
   if ((dev_alloc(c, &md.x, static_cast<size_t>(kMaxRows) * H * 4)) ||
       (dev_alloc(c, &md.yin, static_cast<size_t>(kMaxRows) * p.n_in_max * 4)) ||
       (dev_alloc(c, &md.o, static_cast<size_t>(kMaxRows) * std::max(1, p.o_stride) * 4)) ||
@@ -575,6 +582,7 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
       (dev_alloc(c, &md.tickets, c->tickets_bytes)) ||
       (dev_alloc(c, &md.attn_part, attn_items_max * kMaxQRows * kPartStride * 4)) ||
       (dev_alloc(c, &md.attn_tickets, c->attn_tickets_bytes)) ||
+      (dev_alloc(c, &md.norm_part, static_cast<size_t>(gemm_phases(L)) * kMaxNormSlices * kMaxRows * 4)) ||
       (dev_alloc(c, &md.top_val, nrec * kMaxRows * 4)) ||
       (dev_alloc(c, &md.top_idx, nrec * kMaxRows * 4)) ||
       (dev_alloc(c, &md.page_table, static_cast<size_t>(L.max_seqs) * L.max_pages_per_seq * 4)) ||
@@ -592,6 +600,7 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
     mk_free(c);
     return MK_ERR_CUDA;
   }
+  md.norm_cnt = md.attn_tickets + attn_counters;
   if (cudaMallocHost(&c->sd_host, sizeof(StepDesc)) != cudaSuccess ||
       cudaMallocHost(&c->out_host, (kOutInts + 16) * 4) != cudaSuccess ||
       cudaMallocHost(&c->pt_host, static_cast<size_t>(L.max_seqs) * L.max_pages_per_seq * 4) != cudaSuccess ||
@@ -975,7 +984,7 @@ constexpr int kMaxDevices = 64;
 void* g_static_addr[kMaxDevices] = {nullptr};
 
 struct StaticLayout {
-  size_t md, x, yin, o, h, gu, logits, tickets, attn_part, attn_tickets, top_val, top_idx, out, bar, err,
+  size_t md, x, yin, o, h, gu, logits, tickets, attn_part, attn_tickets, norm_part, top_val, top_idx, out, bar, err,
       attn_scratch, total;
 };
 
@@ -995,6 +1004,7 @@ StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
   take(L.tickets, c->tickets_bytes);
   take(L.attn_part, static_cast<size_t>(std::max(1, n_attn_items)) * kMaxQRows * kPartStride * 4);
   take(L.attn_tickets, c->attn_tickets_bytes);
+  take(L.norm_part, static_cast<size_t>(gemm_phases(c->L)) * kMaxNormSlices * kMaxRows * 4);
   take(L.top_val, nrec * kMaxRows * 4);
   take(L.top_idx, nrec * kMaxRows * 4);
   take(L.out, kOutInts * 4);
@@ -1040,6 +1050,8 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
   md.tickets = reinterpret_cast<uint32_t*>(base + SL.tickets);
   md.attn_part = reinterpret_cast<float*>(base + SL.attn_part);
   md.attn_tickets = reinterpret_cast<uint32_t*>(base + SL.attn_tickets);
+  md.norm_cnt = md.attn_tickets + (c->md_host.norm_cnt - c->md_host.attn_tickets);
+  md.norm_part = reinterpret_cast<float*>(base + SL.norm_part);
   md.top_val = reinterpret_cast<float*>(base + SL.top_val);
   md.top_idx = reinterpret_cast<int32_t*>(base + SL.top_idx);
   md.out = reinterpret_cast<int32_t*>(base + SL.out);

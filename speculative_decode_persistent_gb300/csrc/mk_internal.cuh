@@ -64,6 +64,7 @@ constexpr int kPartStride = kMaxDh + 4;       // floats per query row of a split
 constexpr int kAttnMaxSlots = 16;             // KV staging slots (their mbarriers live in misc)
 constexpr int kAttnBarOff = 3840;             // byte offset of those mbarriers inside misc
 constexpr int kMaxDraft = MK_MAX_T - 1;       // MTP drafts per sequence and step
+constexpr int kMaxNormSlices = 16;            // reduction slices of an RMSNorm GEMM phase
 // the step's own rows plus the draft passes' positions fit one new-rows chunk
 static_assert(kMaxT + kMaxDraft - 1 <= kChunk, "draft positions of one step");
 
@@ -130,6 +131,11 @@ struct ModelDesc {
   uint32_t* tickets; // per tile
   float* attn_part;  // [attn items][kMaxQRows][kPartStride]: dims, then m and l (log2 units)
   uint32_t* attn_tickets;  // per (step sequence, kv head)
+  // RMSNorm row sums of a sliced RMSNorm GEMM phase gp: one partial per
+  // reduction slice (written by the slice's first block), [gp][kMaxNormSlices][kMaxRows],
+  // and per phase the number of slices published (cleared before each launch)
+  float* norm_part;
+  uint32_t* norm_cnt;
   float* top_val;    // [grid*kWarps][kMaxRows]
   int32_t* top_idx;  // [grid*kWarps][kMaxRows]
   int32_t* page_table;     // [max_seqs][max_pages_per_seq]
@@ -237,14 +243,18 @@ __host__ __device__ inline void attn_plan(int q_rows_max, int dh, int q8, int ri
   nslots = spg * ng;
 }
 
+// Sub-block sums of the activation rows: [super-block][sub-block][kSxStride]
+// floats (rows padded to 12, so a math lane reads four rows with one 16-byte load).
+constexpr int kSxStride = kMaxRows;
+
 __host__ __device__ inline int act_bytes(int nsb_slice, int R) {
-  return 2 * R * act_col_stride(nsb_slice) + nsb_slice * 8 * R * 4;  // = 1056 R n + 128 R
+  return 2 * R * act_col_stride(nsb_slice) + nsb_slice * 8 * kSxStride * 4;  // = 1024 R n + 128 R + 384 n
 }
 
 __host__ __device__ inline Sched make_sched(int nsb, int R) {
-  // largest slice with act_bytes(n, R) = 1056 R n + 128 R <= kActBytes
+  // largest slice with act_bytes(n, R) = 1024 R n + 128 R + 384 n <= kActBytes
   Sched s;
-  int max_sb = (kActBytes - 128 * R) / (1056 * R);
+  int max_sb = (kActBytes - 128 * R) / (1024 * R + 8 * kSxStride * 4);
   if (max_sb < 1) max_sb = 1;
   if (max_sb > nsb) max_sb = nsb;
   s.S = (nsb + max_sb - 1) / max_sb;

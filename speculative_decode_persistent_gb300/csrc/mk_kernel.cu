@@ -334,7 +334,8 @@ __device__ void embed_phase(const ModelDesc& md, const StepDesc& sd, const WarpC
 // Fills the activation region for reduction slice [sb0, sb0 + nsb_s): for each
 // row r, column 2r holds the fp16 high part and column 2r+1 the low part of the
 // input vector, each column in the per-32 permuted order of the B fragments;
-// then sx[sb][j][r] = sum of (high + low) over sub-block j. Loads are float4,
+// then sx[sb][j][r] (rows padded to kSxStride) = sum of (high + low) over
+// sub-block j. Loads are float4,
 // and per-row norms reduce over the whole block in a fixed order.
 __device__ __forceinline__ int act_perm(int kl) {
   const int i = kl & 31;
@@ -365,52 +366,7 @@ __device__ __forceinline__ void put_act(__half* act, int cs2, int R, float* sx, 
   part += __shfl_xor_sync(0xffffffffu, part, 1);
   part += __shfl_xor_sync(0xffffffffu, part, 2);
   part += __shfl_xor_sync(0xffffffffu, part, 4);
-  if ((lane & 7) == 0) sx[((kl >> 8) * 8 + ((kl & 255) >> 5)) * R + r] = part;
-}
-
-// 1/rms of every row of the residual stream into misc[r], from the full rows
-// (the residual writers only add into x, so nobody else has the sums): the
-// loads of a batch are all issued before any is used, with the batch sized to
-// the row count (one batch for one row group of 4 at the 27B width).
-template <int NT>
-__device__ __forceinline__ void row_inv_rms(const ModelDesc& md, int R, float* misc, float* red) {
-  constexpr int RB = 4 * NT, JB = NT == 1 ? 6 : NT == 2 ? 3 : 2;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nq4 = md.H / 4;
-  float sq[RB];
-#pragma unroll
-  for (int r = 0; r < RB; ++r) sq[r] = 0.f;
-  for (int j0 = 0; j0 * kThreads < nq4; j0 += JB) {
-    float4 v[RB][JB];
-#pragma unroll
-    for (int r = 0; r < RB; ++r)
-#pragma unroll
-      for (int jj = 0; jj < JB; ++jj) {
-        const int c = (j0 + jj) * kThreads + tid;
-        v[r][jj] = (r < R && c < nq4)
-                       ? __ldcg(reinterpret_cast<const float4*>(md.x + static_cast<size_t>(r) * md.H) + c)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-    for (int r = 0; r < RB; ++r)
-#pragma unroll
-      for (int jj = 0; jj < JB; ++jj)
-        sq[r] = fmaf(v[r][jj].x, v[r][jj].x, fmaf(v[r][jj].y, v[r][jj].y,
-                     fmaf(v[r][jj].z, v[r][jj].z, fmaf(v[r][jj].w, v[r][jj].w, sq[r]))));
-  }
-#pragma unroll
-  for (int r = 0; r < RB; ++r)
-    if (r < R) {
-      const float t = warp_sum(sq[r]);
-      if (lane == 0) red[warp * kMaxRows + r] = t;
-    }
-  math_sync();
-  if (tid < R) {
-    float t = 0.f;
-    for (int w = 0; w < kWarps; ++w) t += red[w * kMaxRows + tid];
-    misc[tid] = 1.0f / sqrtf(t / static_cast<float>(md.H) + md.eps);
-  }
-  math_sync();
+  if ((lane & 7) == 0) sx[((kl >> 8) * 8 + ((kl & 255) >> 5)) * kSxStride + r] = part;
 }
 
 // One round of loads: every thread issues all of its source float4 loads
@@ -422,8 +378,7 @@ __device__ __forceinline__ void row_inv_rms(const ModelDesc& md, int R, float* m
 // kind, so the instructions it executes are contiguous.
 template <int PRO>
 __device__ __forceinline__ void prologue_rounds(const ModelDesc& md, const GemmDesc& g, int R, int k0, int per_row,
-                                                __half* act, int cs2, float* sx, float* misc, float* red,
-                                                bool own_norm) {
+                                                __half* act, int cs2, float* sx, float* red) {
   constexpr int kB = 8;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int total = R * per_row;
@@ -456,20 +411,16 @@ __device__ __forceinline__ void prologue_rounds(const ModelDesc& md, const GemmD
       }
     }
     if constexpr (PRO == PRO_RMS_X) {
-      if (own_norm) {
-        float sq = 0.f;
+      // this slice's sums of squares per row: the 32 float4 of one warp's
+      // load b lie in one row (a row holds a multiple of 64 float4)
 #pragma unroll
-        for (int b = 0; b < kB; ++b)  // elements past the row were loaded as zeros
-          sq = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, fmaf(s1[b].w, s1[b].w, sq))));
-        sq = warp_sum(sq);
-        if (lane == 0) red[warp * kMaxRows] = sq;
-        math_sync();
-        if (tid == 0) {
-          float t = 0.f;
-          for (int w = 0; w < kWarps; ++w) t += red[w * kMaxRows];
-          misc[0] = 1.0f / sqrtf(t / static_cast<float>(md.H) + md.eps);
+      for (int b = 0; b < kB; ++b) {
+        const int idx0 = base + b * kThreads + warp * 32;
+        if (idx0 < total) {
+          float sq = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, s1[b].w * s1[b].w)));
+          sq = warp_sum(sq);
+          if (lane == 0) red[warp * kMaxRows + idx0 / per_row] += sq;
         }
-        math_sync();
       }
     }
 #pragma unroll
@@ -478,10 +429,9 @@ __device__ __forceinline__ void prologue_rounds(const ModelDesc& md, const GemmD
       if (idx < total) {  // warp-uniform: total is a multiple of 64
         const int r = idx / per_row, kl = (idx - r * per_row) * 4, k = k0 + kl;
         float u[4];
-        if constexpr (PRO == PRO_RMS_X) {
+        if constexpr (PRO == PRO_RMS_X) {  // x (.) gain; the row's 1/rms scales the GEMM's outputs
           const float4 gg = s2[b];
-          const float sc = misc[r];
-          u[0] = s1[b].x * sc * gg.x; u[1] = s1[b].y * sc * gg.y; u[2] = s1[b].z * sc * gg.z; u[3] = s1[b].w * sc * gg.w;
+          u[0] = s1[b].x * gg.x; u[1] = s1[b].y * gg.y; u[2] = s1[b].z * gg.z; u[3] = s1[b].w * gg.w;
         } else if constexpr (PRO == PRO_GDN_OUT) {
           float hs = fmaf(s1[b].x, s1[b].x, fmaf(s1[b].y, s1[b].y, fmaf(s1[b].z, s1[b].z, s1[b].w * s1[b].w)));
           for (int off = 1; off < md.dv / 4; off <<= 1) hs += __shfl_xor_sync(0xffffffffu, hs, off);
@@ -506,32 +456,94 @@ __device__ __forceinline__ void prologue_rounds(const ModelDesc& md, const GemmD
   }
 }
 
+constexpr int kTopRecOffFloats = 640;  // per-warp top-1 records inside misc (floats)
+// Per-warp 1/rms of the rows of an RMSNorm GEMM phase, inside misc (floats).
+constexpr int kInvOff = 840;
+static_assert(kInvOff >= kTopRecOffFloats + kWarps * 2 * kMaxRows && (kInvOff + kWarps * kMaxRows) * 4 <= kAttnBarOff,
+              "RMSNorm scales in misc");
+
+// The activation operand of one GEMM phase for this block's reduction slice.
+// An RMSNorm phase feeds x (.) gain and leaves the row's 1/rms to scale the
+// GEMM's outputs (it is one factor per row): with one slice the block's own
+// loads are the whole row, so each warp takes the block's sums of squares;
+// with several, the slice's first block publishes its partial sums and each
+// warp adds the partials of all slices (load_inv) before its first output.
 template <int NT>
-__device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g, int sb0,
-                              int nsb_s, const Smem& sm) {
-  constexpr int kB = 8;
+__device__ void gemm_prologue(const ModelDesc& md, const StepDesc& sd, const GemmDesc& g, int gp, const Assign& a,
+                              const Smem& sm) {
   const int R = sd.R;
-  const int k0 = sb0 * 256, ks = nsb_s * 256;
-  const int cstride = act_col_stride(nsb_s);
+  const int k0 = a.sb0 * 256, ks = a.nsb_s * 256;
+  const int cstride = act_col_stride(a.nsb_s);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __half* act = reinterpret_cast<__half*>(sm.act());
   float* sx = reinterpret_cast<float*>(sm.act() + 2 * R * cstride);
-  float* misc = sm.misc();                        // 1/rms per row
-  float* red = misc + 512;                        // [warp][row] partial sums
+  float* misc = sm.misc();
+  float* red = misc + 512;  // [warp][row] sums of squares of this slice (RMSNorm phases)
   const int per_row = ks / 4;
   const int cs2 = cstride / 2;
-  const int total = R * per_row;
-  // one row whose whole reduction fits one round: the round's own loads are
-  // the full row, so its sum of squares comes from them (no separate batch)
-  const bool own_norm = g.pro == PRO_RMS_X && R == 1 && k0 == 0 && ks == md.H && total <= kThreads * kB;
-  if (g.pro == PRO_RMS_X && !own_norm) row_inv_rms<NT>(md, R, misc, red);
+  if (g.pro == PRO_RMS_X) {
+    if (lane < kMaxRows) red[warp * kMaxRows + lane] = 0.f;
+    __syncwarp();
+  }
   switch (g.pro) {
-    case PRO_RMS_X: prologue_rounds<PRO_RMS_X>(md, g, R, k0, per_row, act, cs2, sx, misc, red, own_norm); break;
-    case PRO_GDN_OUT: prologue_rounds<PRO_GDN_OUT>(md, g, R, k0, per_row, act, cs2, sx, misc, red, false); break;
-    case PRO_FA_OUT: prologue_rounds<PRO_FA_OUT>(md, g, R, k0, per_row, act, cs2, sx, misc, red, false); break;
-    case PRO_MTP_IN: prologue_rounds<PRO_MTP_IN>(md, g, R, k0, per_row, act, cs2, sx, misc, red, false); break;
-    default: prologue_rounds<PRO_H>(md, g, R, k0, per_row, act, cs2, sx, misc, red, false); break;
+    case PRO_RMS_X: prologue_rounds<PRO_RMS_X>(md, g, R, k0, per_row, act, cs2, sx, red); break;
+    case PRO_GDN_OUT: prologue_rounds<PRO_GDN_OUT>(md, g, R, k0, per_row, act, cs2, sx, red); break;
+    case PRO_FA_OUT: prologue_rounds<PRO_FA_OUT>(md, g, R, k0, per_row, act, cs2, sx, red); break;
+    case PRO_MTP_IN: prologue_rounds<PRO_MTP_IN>(md, g, R, k0, per_row, act, cs2, sx, red); break;
+    default: prologue_rounds<PRO_H>(md, g, R, k0, per_row, act, cs2, sx, red); break;
   }
   math_sync();
+  if (g.pro == PRO_RMS_X) {
+    float tot = 0.f;
+    if (lane < R)
+      for (int w = 0; w < kWarps; ++w) tot += red[w * kMaxRows + lane];
+    if (a.sc.S == 1) {
+      if (lane < R) misc[kInvOff + warp * kMaxRows + lane] = 1.0f / sqrtf(tot / static_cast<float>(md.H) + md.eps);
+    } else if (static_cast<int>(blockIdx.x) == a.cta0 && warp == 0) {
+      if (lane < R) md.norm_part[(static_cast<size_t>(gp) * kMaxNormSlices + a.sl) * kMaxRows + lane] = tot;
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(md.norm_cnt + gp) : "memory");
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// A warp's 1/rms of the rows of a sliced RMSNorm phase: a bounded wait until
+// every slice has published its partial sums of squares, then their sum in
+// slice order. False (and the error word set) on timeout or another error.
+__device__ __noinline__ bool load_inv(const ModelDesc& md, const StepDesc& sd, int gp, int S, int warp, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    volatile int32_t* err = md.err;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+      if (ld_acquire(md.norm_cnt + gp) >= static_cast<uint32_t>(S)) break;
+      if ((it & 15u) == 15u) {
+        if (*err != 0) { ok = 0; break; }
+        const uint64_t now = globaltimer();
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > sd.barrier_timeout_ns || it > (1u << 30)) {
+          atomicCAS(md.err, 0, DEV_BARRIER_TIMEOUT);
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return false;
+  if (lane < sd.R) {
+    (void)ld_acquire(md.norm_cnt + gp);  // this lane's own acquire of the published sums
+    float tot = 0.f;
+    for (int sl = 0; sl < S; ++sl) tot += __ldcg(md.norm_part + (static_cast<size_t>(gp) * kMaxNormSlices + sl) * kMaxRows + lane);
+    reinterpret_cast<float*>(smem_raw + kOffMisc)[kInvOff + warp * kMaxRows + lane] =
+        1.0f / sqrtf(tot / static_cast<float>(md.H) + md.eps);
+  }
+  __syncwarp();
+  return true;
 }
 
 // ------------------------------------------------------------- top-1 state
@@ -545,7 +557,7 @@ __device__ __forceinline__ void top1_merge(float& a1, int& ai, float b1, int bi)
 
 // Running top-1 of every row over the lm_head tiles a warp has finished:
 // kMaxRows (value, index) pairs per warp in the misc region.
-constexpr int kTopRecOff = 640;  // float offset inside misc
+constexpr int kTopRecOff = kTopRecOffFloats;  // float offset inside misc
 static_assert((kTopRecOff + kWarps * 2 * kMaxRows) * 4 <= kAttnBarOff, "top-1 records");
 __device__ __forceinline__ float* top_rec(int warp) {
   return reinterpret_cast<float*>(smem_raw + kOffMisc) + kTopRecOff + warp * 2 * kMaxRows;
@@ -615,6 +627,76 @@ __device__ __forceinline__ void gemm_epilogue(const ModelDesc& md, const StepDes
 }
 
 // ------------------------------------------------------------- GEMM phase
+// The math warp may read ring position `pos`: a try-wait on its full barrier,
+// then (rarely) the bounded wait. Inline, so the unit loop makes no call.
+__device__ __forceinline__ bool wait_slot(const Smem& sm, int warp, uint32_t pos, const ModelDesc& md,
+                                          uint64_t timeout_ns) {
+  uint64_t* b = sm.bar(warp, pos % kRing);
+  const uint32_t parity = (pos / kRing) & 1u;
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  volatile int32_t* err = md.err;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*err != 0) return false;
+      if (globaltimer() - t0 > timeout_ns || it > (1u << 26)) {
+        atomicCAS(md.err, 0, DEV_COPY_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// One finished tile segment of an lm_head phase (top-1 records, optional
+// debug dump, completion tickets), out of line: row `lane` of the segment's
+// outputs for every activation row is in stage[lane * 17 + r], already
+// scaled by the rows' 1/rms. A tile the warp computed whole goes straight to
+// its epilogue; a split one is summed by red.add into the logits buffer, and
+// when the reduction is not sliced the last contributor (completion ticket)
+// runs the epilogue on the sum.
+template <int NT, bool TOP>
+__device__ __noinline__ void tile_out_top(const ModelDesc& md, const StepDesc& sd, int gp, uint32_t tile, bool whole,
+                                          const float* stage, int lane, int warp) {
+  const GemmDesc& g = gemm_desc(md, gp);
+  const int R = sd.R;
+  float v[4 * NT];
+#pragma unroll
+  for (int r = 0; r < 4 * NT; ++r) v[r] = r < R ? stage[lane * 17 + r] : 0.f;
+  __syncwarp();
+  if (whole) {
+    gemm_epilogue<NT, TOP>(md, sd, g, tile, v, lane, warp, false);
+    return;
+  }
+  float* dst = md.logits;
+  const int dstride = md.V;
+  const int n = static_cast<int>(tile) * kTileRows + lane;
+  if (n < g.n_out) {
+#pragma unroll
+    for (int r = 0; r < 4 * NT; ++r)
+      if (r < R) atomicAdd(dst + static_cast<size_t>(r) * dstride + n, v[r]);
+  }
+  // sliced logits are scanned by lm_argmax after the next barrier
+  const Sched sc = make_sched(g.nsb, R);
+  if (sc.S > 1) return;
+  __threadfence();
+  __syncwarp();
+  uint32_t last = 0;
+  if (lane == 0) {
+    const uint32_t na = tile_arrivals(sc, g.n_tiles, g.nsb, gridDim.x, tile);
+    const uint32_t old = atomicAdd(&md.tickets[tile], 1u);
+    last = (old + 1u == na) ? 1u : 0u;
+    if (last) md.tickets[tile] = 0u;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+#pragma unroll
+  for (int r = 0; r < 4 * NT; ++r)
+    v[r] = (r < R && n < g.n_out) ? __ldcg(dst + static_cast<size_t>(r) * dstride + n) : 0.f;
+  gemm_epilogue<NT, TOP>(md, sd, g, tile, v, lane, warp, true);
+}
+
 // One word of 8 codes -> the four A registers of a 16x16 block, exactly: a
 // code masked into the low mantissa bits of an fp16 is the subnormal value
 // q * 2^-24 (rows g, nibbles at bits 0-3 / 16-19) or q * 2^-20 (rows g+8,
@@ -629,12 +711,17 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&a)[4]) {
 }
 
 
+// A 6-bit field as an exact float without a conversion instruction: its bits
+// become the low mantissa bits of 2^23, which is then subtracted.
+__device__ __forceinline__ float u6f(uint32_t v) { return __uint_as_float(0x4B000000u | v) - 8388608.0f; }
+
 // One step of the own-row header decode: sub-block j of the lane's row in
 // the next unit -> its fp32 scale d * sc_j * 2^24 (or 2^20), exact, into the
-// scale table, and the min term dmin * m_j * sum_j(x) added into mtmp.
+// scale table, and the min term dmin * m_j * sum_j(x) added into mtmp (four
+// activation rows per 16-byte load of the padded sub-block sums).
 template <int NT>
 __device__ __forceinline__ float decode_step(int j, const uint4& hdr, float dscale, float dmin, const float* sxb,
-                                             int R, float (&mtmp)[4 * NT]) {
+                                             float (&mtmp)[4 * NT]) {
   const uint32_t f0 = hdr.y, f1 = hdr.z, f2 = hdr.w;
   uint32_t sc, m;
   switch (j) {  // 6-bit fields: sc_j at bit 6j, m_j at bit 48 + 6j of the 96-bit field
@@ -647,11 +734,16 @@ __device__ __forceinline__ float decode_step(int j, const uint4& hdr, float dsca
     case 6: sc = (f1 >> 4) & 63u; m = (f2 >> 20) & 63u; break;
     default: sc = (f1 >> 10) & 63u; m = (f2 >> 26) & 63u; break;
   }
-  const float dm = dmin * static_cast<float>(m);  // exact: 11-bit x 6-bit
+  const float dm = dmin * u6f(m);  // exact: 11-bit x 6-bit
 #pragma unroll
-  for (int r = 0; r < 4 * NT; ++r)
-    if (r < R) mtmp[r] = fmaf(dm, sxb[j * R + r], mtmp[r]);
-  return dscale * static_cast<float>(sc);  // exact: 11-bit x 6-bit
+  for (int i = 0; i < NT; ++i) {
+    const float4 sv = *reinterpret_cast<const float4*>(sxb + j * kSxStride + 4 * i);
+    mtmp[4 * i + 0] = fmaf(dm, sv.x, mtmp[4 * i + 0]);
+    mtmp[4 * i + 1] = fmaf(dm, sv.y, mtmp[4 * i + 1]);
+    mtmp[4 * i + 2] = fmaf(dm, sv.z, mtmp[4 * i + 2]);
+    mtmp[4 * i + 3] = fmaf(dm, sv.w, mtmp[4 * i + 3]);
+  }
+  return dscale * u6f(sc);  // exact: 11-bit x 6-bit
 }
 
 // The own row's 8 sub-block scales go to the scale table in one burst, after
@@ -680,7 +772,7 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
     const int cols = g.zero_buf == ZERO_GU ? 2 * md.F : md.n_in_max;
     for (int idx = blockIdx.x * kThreads + threadIdx.x; idx < R * cols; idx += grid * kThreads) zp[idx] = 0.f;
   }
-  gemm_prologue<NT>(md, sd, g, a.sb0, a.nsb_s, sm);
+  gemm_prologue<NT>(md, sd, g, gp, a, sm);
 
   const int lane = wc.lane, gq = lane >> 2, cq = lane & 3;
   const int cstride = act_col_stride(a.nsb_s);
@@ -696,14 +788,6 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
   const uint8_t* bcol[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) bcol[nt] = act + min(nt * 8 + gq, 2 * R - 1) * cstride + cq * 16;
-  // where split tiles are summed
-  float* dst = g.epi == EPI_STORE_YIN ? md.yin : g.epi == EPI_RESID_X ? md.x : g.epi == EPI_STORE_GU ? md.gu : md.logits;
-  const int dstride = g.epi == EPI_STORE_YIN ? md.n_in_max : g.epi == EPI_RESID_X ? md.H
-                      : g.epi == EPI_STORE_GU ? 2 * md.F : md.V;
-  // stores, residual adds and split logits need no completion step: the
-  // summed buffer is the output (the next RMSNorm takes its row sums from the
-  // full rows; split logits are scanned by lm_argmax after the next barrier)
-  const bool no_ticket = g.epi == EPI_STORE_YIN || g.epi == EPI_STORE_GU || g.epi == EPI_RESID_X || (TOP && a.sc.S > 1);
   if (TOP) {
     float* rec = top_rec(wc.warp);
     if (lane < R) {
@@ -715,7 +799,6 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
 
   float acc[2][NT][4];
   float mn[4 * NT], mtmp[4 * NT];
-  uint32_t seg_u0 = a.u0;
 #pragma unroll
   for (int rb = 0; rb < 2; ++rb)
 #pragma unroll
@@ -723,70 +806,28 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[rb][nt][e] = 0.f;
 
-  auto flush = [&](uint32_t tile, uint32_t u_end, float* stage) {
-    __syncwarp();
-#pragma unroll
-    for (int rb = 0; rb < 2; ++rb)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int r = nt * 4 + cq;
-        if (r < R) {
-          stage[(rb * 16 + gq) * 17 + r] = acc[rb][nt][0] + acc[rb][nt][1];
-          stage[(rb * 16 + gq + 8) * 17 + r] = acc[rb][nt][2] + acc[rb][nt][3];
-        }
-      }
-    __syncwarp();
-    float v[4 * NT];
-#pragma unroll
-    for (int r = 0; r < 4 * NT; ++r) v[r] = r < R ? stage[lane * 17 + r] - mn[r] : 0.f;
-    __syncwarp();
-    const uint32_t tu0 = tile * nsb_s, tu1 = tu0 + nsb_s;
-    if (a.sc.S == 1 && seg_u0 == tu0 && u_end == tu1 && g.epi != EPI_RESID_X) {  // the whole tile: no one else contributes
-      gemm_epilogue<NT, TOP>(md, sd, g, tile, v, lane, wc.warp, false);
-      return;
-    }
-    const int n = static_cast<int>(tile) * kTileRows + lane;
-    if (n < g.n_out) {
-#pragma unroll
-      for (int r = 0; r < 4 * NT; ++r)
-        if (r < R) atomicAdd(dst + static_cast<size_t>(r) * dstride + n, v[r]);
-    }
-    if (no_ticket) return;
-    __threadfence();
-    __syncwarp();
-    uint32_t last = 0;
-    if (lane == 0) {
-      const uint32_t na = tile_arrivals(a.sc, g.n_tiles, g.nsb, grid, tile);
-      const uint32_t old = atomicAdd(&md.tickets[tile], 1u);
-      last = (old + 1u == na) ? 1u : 0u;
-      if (last) md.tickets[tile] = 0u;
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
-#pragma unroll
-    for (int r = 0; r < 4 * NT; ++r)
-      v[r] = (r < R && n < g.n_out) ? __ldcg(dst + static_cast<size_t>(r) * dstride + n) : 0.f;
-    gemm_epilogue<NT, TOP>(md, sd, g, tile, v, lane, wc.warp, true);
-  };
-
+  // where this phase's outputs go (stores of whole tiles, red.add of split ones)
+  float* const dst = g.epi == EPI_STORE_YIN ? md.yin : g.epi == EPI_RESID_X ? md.x : md.gu;
+  const int dstride = g.epi == EPI_STORE_YIN ? md.n_in_max : g.epi == EPI_RESID_X ? md.H : 2 * md.F;
+  const bool rms = g.pro == PRO_RMS_X;
   bool ok = true;
+  bool inv_ready = !rms || a.sc.S == 1;
   if (a.u1 > a.u0) {
     uint32_t tile = a.u0 / nsb_s;
     int sbl = static_cast<int>(a.u0 - tile * nsb_s);
-    // pipeline fill: decode the first unit
+    uint32_t seg_u0 = a.u0;
+    // pipeline fill: the first unit's own-row scales into table 0, its min term into mn
 #pragma unroll
     for (int r = 0; r < 4 * NT; ++r) mtmp[r] = 0.f;
-    if (!wait_unit(wc, sm, md, sd.barrier_timeout_ns)) {
+    if (!wait_slot(sm, wc.warp, wc.c_pos, md, sd.barrier_timeout_ns)) {
       ok = false;
     } else {
-      const uint8_t* unit = sm.ring(wc.warp, wc.c_pos % kRing);
-      const uint4 hdr = *reinterpret_cast<const uint4*>(unit + 16 * lane);
+      const uint4 hdr = *reinterpret_cast<const uint4*>(sm.ring(wc.warp, wc.c_pos % kRing) + 16 * lane);
       const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xffffu)));
       const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
       float scl[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) scl[j] = decode_step<NT>(j, hdr, d * row_unscale, dmin, sx + sbl * 8 * R, R, mtmp);
+      for (int j = 0; j < 8; ++j) scl[j] = decode_step<NT>(j, hdr, d * row_unscale, dmin, sx + sbl * 8 * kSxStride, mtmp);
       store_scales(reinterpret_cast<float*>(sm.stab(wc.warp, 0)), scl, og, orb, ohi);
     }
 #pragma unroll
@@ -795,25 +836,21 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
     for (uint32_t u = a.u0; ok && u < a.u1; ++u) {
       const int cur = static_cast<int>((u - a.u0) & 1u);
       const bool has_next = u + 1 < a.u1;
-      const int sbl_next = sbl + 1 == nsb_s ? 0 : sbl + 1;
+      if (has_next && !wait_slot(sm, wc.warp, wc.c_pos + 1, md, sd.barrier_timeout_ns)) { ok = false; break; }
       const uint8_t* unit = sm.ring(wc.warp, wc.c_pos % kRing);
+      // the next unit's header (the current one's when this is the last: decoded, never used)
+      const uint4 hdrn =
+          *reinterpret_cast<const uint4*>(sm.ring(wc.warp, (wc.c_pos + (has_next ? 1u : 0u)) % kRing) + 16 * lane);
+      const float dscalen = __half2float(__ushort_as_half(static_cast<unsigned short>(hdrn.x & 0xffffu))) * row_unscale;
+      const float dminn = __half2float(__ushort_as_half(static_cast<unsigned short>(hdrn.x >> 16)));
+      const int sbl_next = sbl + 1 == nsb_s ? 0 : sbl + 1;
       const float* tab = reinterpret_cast<const float*>(sm.stab(wc.warp, cur));
       float* tabn = reinterpret_cast<float*>(sm.stab(wc.warp, cur ^ 1));
-      uint4 hdrn = make_uint4(0u, 0u, 0u, 0u);
-      float dscalen = 0.f, dminn = 0.f;
-      if (has_next) {
-        WarpCtx nx = wc;
-        ++nx.c_pos;
-        if (!wait_unit(nx, sm, md, sd.barrier_timeout_ns)) { ok = false; break; }
-        hdrn = *reinterpret_cast<const uint4*>(sm.ring(wc.warp, nx.c_pos % kRing) + 16 * lane);
-        dscalen = __half2float(__ushort_as_half(static_cast<unsigned short>(hdrn.x & 0xffffu))) * row_unscale;
-        dminn = __half2float(__ushort_as_half(static_cast<unsigned short>(hdrn.x >> 16)));
-      }
 #pragma unroll
       for (int r = 0; r < 4 * NT; ++r) mtmp[r] = 0.f;
       const uint8_t* codes = unit + kUnitHdr + lane * 16;
       const int boff = sbl * 512;
-      const float* sxn = sx + sbl_next * 8 * R;
+      const float* sxn = sx + sbl_next * 8 * kSxStride;
       float scl[8];
 #pragma unroll
       for (int kp = 0; kp < 8; ++kp) {
@@ -825,52 +862,76 @@ __device__ __noinline__ bool gemm_phase(const ModelDesc& md, const StepDesc& sd,
         for (int nt = 0; nt < NT; ++nt)
           bf[nt] = *reinterpret_cast<const uint4*>(bcol[nt] + boff + kp * 64);
         uint32_t av[4];
-        {  // rows 0..15 of the tile: words x (k-step 0) and z (k-step 1)
+#pragma unroll
+        for (int rb = 0; rb < 2; ++rb) {  // rows 16rb..16rb+15: words x/z (rb 0) or y/w (rb 1)
           float t[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) t[nt][e] = 0.f;
-          dequant_word(w4.x, av);
+          dequant_word(rb ? w4.y : w4.x, av);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816(t[nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
-          dequant_word(w4.z, av);
+          dequant_word(rb ? w4.w : w4.z, av);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816(t[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
+          const float sa = rb ? s4.z : s4.x, sb = rb ? s4.w : s4.y;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            acc[0][nt][0] = fmaf(s4.x, t[nt][0], acc[0][nt][0]);
-            acc[0][nt][1] = fmaf(s4.x, t[nt][1], acc[0][nt][1]);
-            acc[0][nt][2] = fmaf(s4.y, t[nt][2], acc[0][nt][2]);
-            acc[0][nt][3] = fmaf(s4.y, t[nt][3], acc[0][nt][3]);
+            acc[rb][nt][0] = fmaf(sa, t[nt][0], acc[rb][nt][0]);
+            acc[rb][nt][1] = fmaf(sa, t[nt][1], acc[rb][nt][1]);
+            acc[rb][nt][2] = fmaf(sb, t[nt][2], acc[rb][nt][2]);
+            acc[rb][nt][3] = fmaf(sb, t[nt][3], acc[rb][nt][3]);
           }
         }
-        {  // rows 16..31: words y and w
-          float t[NT][4];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) t[nt][e] = 0.f;
-          dequant_word(w4.y, av);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816(t[nt], av[0], av[1], av[2], av[3], bf[nt].x, bf[nt].y);
-          dequant_word(w4.w, av);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816(t[nt], av[0], av[1], av[2], av[3], bf[nt].z, bf[nt].w);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            acc[1][nt][0] = fmaf(s4.z, t[nt][0], acc[1][nt][0]);
-            acc[1][nt][1] = fmaf(s4.z, t[nt][1], acc[1][nt][1]);
-            acc[1][nt][2] = fmaf(s4.w, t[nt][2], acc[1][nt][2]);
-            acc[1][nt][3] = fmaf(s4.w, t[nt][3], acc[1][nt][3]);
-          }
-        }
-        scl[kp] = has_next ? decode_step<NT>(kp, hdrn, dscalen, dminn, sxn, R, mtmp) : 0.f;
+        scl[kp] = decode_step<NT>(kp, hdrn, dscalen, dminn, sxn, mtmp);
       }
-      if (has_next) store_scales(tabn, scl, og, orb, ohi);
+      store_scales(tabn, scl, og, orb, ohi);
       release_unit(wc, sm);  // includes __syncwarp: both tables are settled
       if (++sbl == nsb_s || u + 1 == a.u1) {
-        flush(tile, u + 1, reinterpret_cast<float*>(sm.stab(wc.warp, cur)));
+        // the tile segment ends: transpose the warp's outputs through the
+        // table just consumed (row = lane), subtract the min term, scale an
+        // RMSNorm phase's rows by their 1/rms, and store or red.add them
+        float* stage = reinterpret_cast<float*>(sm.stab(wc.warp, cur));
+#pragma unroll
+        for (int rb = 0; rb < 2; ++rb)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int r = nt * 4 + cq;
+            if (r < R) {
+              stage[(rb * 16 + gq) * 17 + r] = acc[rb][nt][0] + acc[rb][nt][1];
+              stage[(rb * 16 + gq + 8) * 17 + r] = acc[rb][nt][2] + acc[rb][nt][3];
+            }
+          }
+        if (!inv_ready) {  // a sliced RMSNorm phase: every slice's row sums, once
+          if (!load_inv(md, sd, gp, a.sc.S, wc.warp, lane)) { ok = false; break; }
+          inv_ready = true;
+        }
+        __syncwarp();
+        const uint32_t tu0 = tile * nsb_s;
+        const bool whole = a.sc.S == 1 && seg_u0 == tu0 && u + 1 == tu0 + nsb_s && g.epi != EPI_RESID_X;
+        const float* inv = reinterpret_cast<const float*>(smem_raw + kOffMisc) + kInvOff + wc.warp * kMaxRows;
+        if (TOP) {
+#pragma unroll
+          for (int r = 0; r < 4 * NT; ++r)
+            if (r < R) stage[lane * 17 + r] = (stage[lane * 17 + r] - mn[r]) * inv[r];
+          __syncwarp();
+          tile_out_top<NT, TOP>(md, sd, gp, tile, whole, stage, lane, wc.warp);
+        } else {
+          const int n = static_cast<int>(tile) * kTileRows + lane;
+          if (n < g.n_out) {
+#pragma unroll
+            for (int r = 0; r < 4 * NT; ++r)
+              if (r < R) {
+                float vr = stage[lane * 17 + r] - mn[r];
+                if (rms) vr *= inv[r];
+                float* p = dst + static_cast<size_t>(r) * dstride + n;
+                if (whole) *p = vr;
+                else atomicAdd(p, vr);
+              }
+          }
+          __syncwarp();
+        }
         seg_u0 = u + 1;
 #pragma unroll
         for (int rb = 0; rb < 2; ++rb)
@@ -2137,6 +2198,11 @@ __device__ __noinline__ void draft_phase(const ModelDesc& md, const StepDesc& sd
 }
 
 // ------------------------------------------------------------ the producer
+#ifndef MK_PRODUCER_NAP
+#define MK_PRODUCER_NAP 0
+#endif
+constexpr unsigned kProducerNapNs = MK_PRODUCER_NAP;  // producer back-off when every ring is full (ns)
+
 // Lanes 0..kWarps-1 each walk one math warp's unit sequence; the warp stays
 // converged: every sweep, each lane issues its next unit if that unit's slot
 // has been released, then the sweep repeats until every lane is done. Before
@@ -2211,8 +2277,13 @@ __device__ __noinline__ void producer_warp(const ModelDesc& md, const StepDesc& 
     }
     if (__any_sync(0xffffffffu, issued)) {
       t_idle = 0;
-    } else if ((sweep & 63u) == 63u) {
-      // nothing could be issued: the math warps are behind; give up only on
+      continue;
+    }
+    // nothing could be issued: the math warps are behind; nap so that the
+    // polling does not take issue slots from the math warps on this SMSP
+    if (kProducerNapNs > 0) __nanosleep(kProducerNapNs);
+    if ((sweep & 63u) == 63u) {
+      // give up only on
       // an error or after the deadline
       if (*err != 0) break;
       const uint64_t now = globaltimer();
