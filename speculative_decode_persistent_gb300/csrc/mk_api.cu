@@ -567,6 +567,8 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
   }
   md.gdn_state = b->gdn_state; md.conv_state = b->conv_state;
 
+  md.part_rows = std::min(kMaxQRows, kMaxT * (L.fa_hq / std::max(1, L.fa_hkv)));
+  md.part_stride = std::max(1, L.fa_dh) + 4;
   const size_t nrec = static_cast<size_t>(c->grid) * kWarps;
   const size_t attn_items_max = static_cast<size_t>(2 * c->grid + kMaxSeqs * std::max(1, L.fa_hkv));
   c->tickets_bytes = static_cast<size_t>(max_tiles) * 4;
@@ -580,7 +582,7 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
       (dev_alloc(c, &md.gu, static_cast<size_t>(kMaxRows) * 2 * F * 4)) ||
       (dev_alloc(c, &md.logits, static_cast<size_t>(kMaxRows) * L.vocab * 4)) ||
       (dev_alloc(c, &md.tickets, c->tickets_bytes)) ||
-      (dev_alloc(c, &md.attn_part, attn_items_max * kMaxQRows * kPartStride * 4)) ||
+      (dev_alloc(c, &md.attn_part, attn_items_max * kMaxAttnGroups * md.part_rows * md.part_stride * 4)) ||
       (dev_alloc(c, &md.attn_tickets, c->attn_tickets_bytes)) ||
       (dev_alloc(c, &md.norm_part, static_cast<size_t>(gemm_phases(L)) * kMaxNormSlices * kMaxRows * 4)) ||
       (dev_alloc(c, &md.top_val, nrec * kMaxRows * 4)) ||
@@ -869,12 +871,17 @@ mk_status mk_step_prepare(mk_ctx* c, int32_t n_rows, const int32_t* tokens, cons
   }
   sd.n_attn_items = items;
   // the splits of one (sequence, kv head) wait for each other before merging:
-  // every item needs a block of its own
-  if (items > c->grid) return MK_ERR_UNSUPPORTED;
+  // every item needs a block of its own; an item's page ids fit the block's page list
+  if (items > c->grid || cps > kAttnPageList) return MK_ERR_UNSUPPORTED;
   if (L.fa_dh > 0) {
-    attn_plan(t_max * (L.fa_hq / hkv), L.fa_dh, L.kv_dtype == MK_KV_Q8, kRingBytes, sd.attn_dsplit, sd.attn_wpg,
-              sd.attn_ng, sd.attn_spg, sd.attn_nslots);
+    attn_plan(t_max * (L.fa_hq / hkv), L.fa_dh, L.kv_dtype == MK_KV_Q8, kRingBytes, sd.attn_nq, sd.attn_jw,
+              sd.attn_wpg, sd.attn_ng, sd.attn_spg, sd.attn_nslots);
     if (sd.attn_spg < 1) return MK_ERR_UNSUPPORTED;
+    // the merge's weights of every (sequence, kv head) fit below the phase's flag word
+    for (int i = 0; i < n_seq; ++i) {
+      const int qrows = T[i] * (L.fa_hq / hkv), parts = sd.seq_nsplit[i] * sd.attn_ng;
+      if (2 * qrows * parts + qrows > kAttnCombineFloats) return MK_ERR_UNSUPPORTED;
+    }
   }
   sd.skip_block = c->skip_block;
   sd.skip_barrier = c->skip_barrier;
@@ -1002,7 +1009,7 @@ StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
   take(L.gu, static_cast<size_t>(kMaxRows) * 2 * md.F * 4);
   take(L.logits, static_cast<size_t>(kMaxRows) * md.V * 4);
   take(L.tickets, c->tickets_bytes);
-  take(L.attn_part, static_cast<size_t>(std::max(1, n_attn_items)) * kMaxQRows * kPartStride * 4);
+  take(L.attn_part, static_cast<size_t>(std::max(1, n_attn_items)) * kMaxAttnGroups * md.part_rows * md.part_stride * 4);
   take(L.attn_tickets, c->attn_tickets_bytes);
   take(L.norm_part, static_cast<size_t>(gemm_phases(c->L)) * kMaxNormSlices * kMaxRows * 4);
   take(L.top_val, nrec * kMaxRows * 4);

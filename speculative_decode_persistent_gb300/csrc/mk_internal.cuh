@@ -60,9 +60,12 @@ constexpr int kMaxDh = 256;
 constexpr int kMaxQRows = 48;                 // T x (hq/hkv) rows attending one kv head
 constexpr int kMaxSplits = 128;               // split-K parts of one (sequence, kv head)
 constexpr int kChunk = 16;                    // cached tokens per attention chunk (one KV page)
-constexpr int kPartStride = kMaxDh + 4;       // floats per query row of a split partial: dims, m, l, pad
 constexpr int kAttnMaxSlots = 16;             // KV staging slots (their mbarriers live in misc)
 constexpr int kAttnBarOff = 3840;             // byte offset of those mbarriers inside misc
+// The page ids of a block's attention item, loaded once by the producer at the
+// start of the item's KV stream, live at the end of the ring region.
+constexpr int kAttnPageList = 512;            // chunks (pages) of one attention item, at most
+constexpr int kAttnPageListBytes = kAttnPageList * 4;
 constexpr int kMaxDraft = MK_MAX_T - 1;       // MTP drafts per sequence and step
 constexpr int kMaxNormSlices = 16;            // reduction slices of an RMSNorm GEMM phase
 // the step's own rows plus the draft passes' positions fit one new-rows chunk
@@ -129,7 +132,8 @@ struct ModelDesc {
   float* gu;         // [kMaxRows][2F] gate/up outputs, 16-row blocks of 8 gate + 8 up rows
   float* logits;     // [kMaxRows][V] lm_head outputs of split tiles (summed by red.add)s
   uint32_t* tickets; // per tile
-  float* attn_part;  // [attn items][kMaxQRows][kPartStride]: dims, then m and l (log2 units)
+  float* attn_part;  // [attn items][kMaxAttnGroups][part_rows][part_stride]: dims, then m and l (log2 units)
+  int32_t part_rows, part_stride;  // query rows of one (sequence, kv head) at most; dh + 4
   uint32_t* attn_tickets;  // per (step sequence, kv head)
   // RMSNorm row sums of a sliced RMSNorm GEMM phase gp: one partial per
   // reduction slice (written by the slice's first block), [gp][kMaxNormSlices][kMaxRows],
@@ -164,8 +168,8 @@ struct StepDesc {
   int32_t seq_prompt[kMaxSeqs];
   int32_t seq_slot_out[kMaxSeqs][kMaxT];
   int32_t seq_nsplit[kMaxSeqs], seq_chunks_per_split[kMaxSeqs], seq_item0[kMaxSeqs];
-  // attention plan of this step (attn_plan): warp groups and KV staging slots
-  int32_t attn_dsplit, attn_wpg, attn_ng, attn_spg, attn_nslots;
+  // attention plan of this step (attn_plan): query n-tiles, warp groups and KV staging slots
+  int32_t attn_nq, attn_jw, attn_wpg, attn_ng, attn_spg, attn_nslots;
   int32_t skip_block, skip_barrier;
   uint64_t barrier_timeout_ns;
   float2 rope[kMaxRows][kMaxDh / 2];  // (cos, sin) of position * base^(-2i/dh)
@@ -225,23 +229,65 @@ __host__ __device__ inline AttnSlot attn_slot_layout(int dh, int q8) {
   return L;
 }
 
-// Warp groups of the attention phase. A warp owns one n-tile of 8 query rows
-// (of the T x hq/hkv rows attending one kv head) and 1/dsplit of the head
-// dimension; the wpg warps covering all n-tiles form a group that consumes
-// one chunk at a time; ng groups take a CTA item's chunks round-robin.
-__host__ __device__ inline void attn_plan(int q_rows_max, int dh, int q8, int ring_bytes, int32_t& dsplit,
-                                          int32_t& wpg, int32_t& ng, int32_t& spg, int32_t& nslots) {
-  const int nq = (q_rows_max + 7) / 8;
-  dsplit = (nq <= 2 && (dh / 16) % 2 == 0) ? 2 : 1;
-  wpg = nq * dsplit;
-  ng = kWarps / wpg;
-  if (ng < 1) ng = 1;
+// Shared memory of the attention phase (the phase region): Q in binary16
+// (8 nq rows of dh + 8 halves), the step's own rows as one more slot, the
+// groups' score-exchange buffers from attn_xoff on, and a flag word at the end.
+__host__ __device__ constexpr int attn_qbytes(int nq, int dh) { return (nq * 8 * (dh + 8) * 2 + 255) / 256 * 256; }
+__host__ __device__ inline int attn_xoff(int nq, int dh, int q8) {
+  return attn_qbytes(nq, dh) + (attn_slot_layout(dh, q8).tx_bytes + 255) / 256 * 256;
+}
+
+// Warp groups of the attention phase. A group of wpg warps takes attn_nu(nq, q8)
+// chunks (16 tokens each) per step. Warp dp of a group owns the head dims of
+// the 32-dim blocks dp*jw .. dp*jw+jw-1 (jw = dh / 32 / wpg) for every query
+// n-tile (8 of the T x hq/hkv rows attending one kv head): it forms those
+// dims' share of the scores and adds P V for the same dims, so each K and V
+// element is read and converted by one warp and used for every n-tile. The
+// softmax of n-tile q is taken by warp q % wpg alone, from the other warps'
+// shares, and handed back as binary16 P fragments and rescale factors. jw
+// is the largest power of two up to attn_jw(nq) that divides dh / 32 (a
+// warp's accumulators: nq x 2 jw m-tiles of 16 dims); the kernel variant is
+// chosen by (nq, jw). ng groups take a block's chunks round-robin, each with
+// at least two staging slots, and each writes its own partial.
+constexpr int kMaxAttnGroups = 8;
+__host__ __device__ constexpr int attn_jw(int nq) { return nq <= 1 ? 4 : nq <= 3 ? 2 : 1; }
+// (two chunks a step take more registers: not for the q8 variant of three n-tiles)
+__host__ __device__ constexpr int attn_nu(int nq, int q8) { return (nq <= 2 || nq == 4 || (nq == 3 && !q8)) ? 2 : 1; }
+// exchange area of one group, in bytes: score shares [wpg-1][nu][nq][32]
+// float4, P fragments [nq][nu][32] uint2, factors [nq][32] float2, sums
+// [nq][4] float2, and the owners' running state [nq][32] float4
+__host__ __device__ constexpr int attn_xslab(int wpg, int nq, int q8) {
+  return (wpg - 1) * attn_nu(nq, q8) * nq * 512 + nq * attn_nu(nq, q8) * 256 + nq * 256 + nq * 32 + nq * 512;
+}
+
+__host__ __device__ inline void attn_plan(int q_rows_max, int dh, int q8, int ring_bytes, int32_t& nq,
+                                          int32_t& jw, int32_t& wpg, int32_t& ng, int32_t& spg,
+                                          int32_t& nslots) {
+  nq = (q_rows_max + 7) / 8;
+  const int nblk = dh / 32;
+  jw = attn_jw(nq);
+  while (nblk % jw) jw /= 2;
+  wpg = nblk / jw;
   const AttnSlot L = attn_slot_layout(dh, q8);
-  nslots = (ring_bytes - 1024) / L.bytes;  // room for aligning the first slot to 1024 bytes
+  // room for aligning the first slot to 1024 bytes, and for the page list after the slots
+  nslots = (ring_bytes - 1024 - kAttnPageListBytes) / L.bytes;
   if (nslots > kAttnMaxSlots) nslots = kAttnMaxSlots;
+  ng = kWarps / wpg;
+  if (ng > nslots / 2) ng = nslots / 2;
+  if (ng > kMaxAttnGroups) ng = kMaxAttnGroups;
+  if (ng < 1) ng = 1;
+  const int room = kPhaseBytes - 16 - attn_xoff(nq, dh, q8);
+  while (ng > 1 && ng * attn_xslab(wpg, nq, q8) > room) --ng;
+  if (ng * attn_xslab(wpg, nq, q8) > room) {  // no plan: the step is refused
+    spg = nslots = 0;
+    return;
+  }
   spg = nslots / ng;
   nslots = spg * ng;
 }
+
+// Floats of the merge's weights below the attention phase's flag word.
+constexpr int kAttnCombineFloats = (kPhaseBytes - 16) / 4;
 
 // Sub-block sums of the activation rows: [super-block][sub-block][kSxStride]
 // floats (rows padded to 12, so a math lane reads four rows with one 16-byte load).

@@ -1324,6 +1324,15 @@ __device__ bool attn_stream(const ModelDesc& md, const StepDesc& sd, const Smem&
     }
   };
   seek();
+  // the block's own item (at most one per block): all of its page ids at
+  // once, so that issuing a page waits for no page-table round trip
+  int* plist = reinterpret_cast<int*>(smem_raw + kOffRing + kRingBytes - kAttnPageListBytes);
+  if (static_cast<int>(blockIdx.x) < sd.n_attn_items) {
+    const AttnItem own = attn_item(sd, hkv, blockIdx.x);
+    const int* src = md.page_table + static_cast<size_t>(sd.seq_id[own.si]) * md.max_pages_per_seq + own.cb;
+    for (int c = lane; c < own.nch && c < kAttnPageList; c += 32) plist[c] = __ldcg(src + c);
+  }
+  __syncwarp();
   volatile int32_t* err = md.err;
   uint64_t t_idle = 0;
   bool ok = true;
@@ -1333,7 +1342,9 @@ __device__ bool attn_stream(const ModelDesc& md, const StepDesc& sd, const Smem&
     if (!done) {
       const int slot = lane * spg + static_cast<int>(kv_issued % static_cast<uint32_t>(spg));
       if (mbar_test(ab.empty + slot, ((kv_issued / spg) & 1u) ^ 1u)) {
-        const int page = md.page_table[static_cast<size_t>(sd.seq_id[it.si]) * md.max_pages_per_seq + it.cb + i];
+        const int page = (item == static_cast<int>(blockIdx.x) && i < kAttnPageList)
+                             ? plist[i]
+                             : md.page_table[static_cast<size_t>(sd.seq_id[it.si]) * md.max_pages_per_seq + it.cb + i];
         const int row = ((fa_i * md.n_pages + page) * hkv + it.kh) * kChunk;
         uint8_t* dst = ab.slots + slot * SL.bytes;
         uint64_t* fb = ab.full + slot;
@@ -1370,49 +1381,107 @@ __device__ bool attn_stream(const ModelDesc& md, const StepDesc& sd, const Smem&
   return __all_sync(0xffffffffu, ok);
 }
 
-struct AttnState {
-  float m[2], l[2];             // running max and sum of query columns 2c, 2c+1
-  float acc[kMaxDh / 16][4];    // O^T: m-tile (16 dims) x (dim rows g, g+8) x (columns 2c, 2c+1)
+// The O^T accumulators of one warp: NQ n-tiles of 8 query rows each, MT
+// m-tiles of 16 head dims (the warp's share of dh).
+template <int NQ, int MT>
+struct AttnAcc {
+  float acc[NQ][MT][4];  // O^T: (dim rows g, g+8) x (columns 2c, 2c+1)
 };
 
-// One chunk for one warp: K rows at kb, V rows at vb (slot layout), q8 block
-// scales at ks / vs. Tokens >= nvalid are masked; causal_grp > 0 also masks
-// token t for query row q when t > q / causal_grp (the step's own rows).
-// Scores are in log2 units (Q carries log2(e) / sqrt(dh)). SWZ: 128-byte
-// swizzled boxes (always for fp16; q8 when dh is a multiple of 128).
-template <bool Q8, bool SWZ>
-__device__ __forceinline__ void attn_chunk(const uint8_t* kb, const uint8_t* vb, const __half* ks, const __half* vs,
-                                           const __half* Qp, int qstride, int dh, int nt, int mt0, int nmt,
-                                           int nvalid, int causal_grp, int lane, AttnState& st) {
+// 2^x by the MUFU instruction (ex2.approx.ftz: relative error near 2^-22,
+// far below the binary16 rounding of P; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kAttnLazy = 8.f;
+
+__device__ __forceinline__ void group_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// One staged chunk of 16 tokens: the slot (or the step's own rows), the
+// tokens that hold data, and the causal group (> 0: token t is masked for
+// query row q when t > q / causal).
+struct AttnSub {
+  const uint8_t* cb;
+  int nvalid, causal;
+};
+
+// A group's exchange area (attn_xslab bytes): score shares, P fragments,
+// rescale factors and the final sums.
+template <int NQ, int NU>
+struct AttnX {
+  float4* s;  // [wpg-1][NU][NQ][32]: the shares of the non-owners, in warp order
+  uint2* p;   // [NQ][NU][32]: P^T fragments (binary16, transposed) of each chunk
+  float2* f;  // [NQ][32]: rescale factors of columns 2c, 2c+1
+  float2* l;  // [NQ][4]: final sums of columns 2c, 2c+1
+  float4* m;  // [NQ][32]: the owner's running max and its lane's share of the sum
+              // (m of columns 2c, 2c+1, then l of columns 2c, 2c+1)
+  __device__ __forceinline__ AttnX(uint8_t* base, int wpg) {
+    s = reinterpret_cast<float4*>(base);
+    p = reinterpret_cast<uint2*>(base + (wpg - 1) * NU * NQ * 512);
+    f = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(p) + NQ * NU * 256);
+    l = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(f) + NQ * 256);
+    m = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(l) + NQ * 32);
+  }
+};
+
+// One step of warp dp of a group of wpg warps over NU chunks. The warp owns
+// the 32-dim blocks j0 .. j0+JW-1 and forms their share of S^T = K Q^T for
+// all NQ query n-tiles (rows past the item's own are zero and are not
+// written out) and every chunk. The softmax of n-tile q is taken by warp
+// q % wpg: it adds the shares (its own, then the others' in warp order),
+// masks, takes the online-softmax step over the NU x 16 tokens and hands the
+// group binary16 P^T fragments and the rescale factors; every warp then
+// rescales its O^T and adds P V for the m-tiles of its blocks. bar_id is the
+// group's named barrier (two per step). Slot layout (SL): K rows, V rows, q8
+// block scales. Scores are in log2 units (Q carries log2(e) / sqrt(dh)).
+// SWZ: 128-byte swizzled boxes (always for fp16; q8 when dh is a multiple of 128).
+template <bool Q8, bool SWZ, int NQ, int JW, int NU>
+__device__ __forceinline__ void attn_chunk(const AttnSub (&sub)[NU], const AttnSlot& SL, const __half* Qp,
+                                           int qstride, int dh, int j0, int lane, int wpg, int dp,
+                                           const AttnX<NQ, NU>& X, int bar_id, AttnAcc<NQ, 2 * JW>& st) {
   constexpr int BW = SWZ ? 128 : 64;  // bytes per box row
   constexpr int BB = kChunk * BW;     // bytes per box
+  // with one chunk and one n-tile, the odd 32-dim blocks go to a second chain (latency)
+  constexpr int NS = (NU == 1 && NQ == 1 && JW > 1) ? 2 : 1;
   const int g = lane >> 2, c = lane & 3;
   const int nblk = dh / 32;
-  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd j chains
-  const __half* qa = Qp + (nt * 8 + (lane & 7)) * qstride + 8 * (lane >> 3);
-  if (!Q8) {
-    // lane c reads the 16-byte chunks 2c and 2c+1 of its box rows in turn
-    const uint8_t* kr0 = kb + g * 128 + (((2 * c) ^ g) << 4);
-    const uint8_t* kr1 = kb + g * 128 + (((2 * c + 1) ^ g) << 4);
-#pragma unroll 4
-    for (int j = 0; j < kMaxDh / 32; ++j) {
-      if (j < nblk) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(b0, b1, b2, b3, qa + 32 * j);
-        const uint8_t* kr = ((j & 1) ? kr1 : kr0) + (j >> 1) * BB;
+  const int nthr = wpg * 32;
+  float s[NU][NS][NQ][4];
+#pragma unroll
+  for (int u = 0; u < NU; ++u)
+#pragma unroll
+    for (int h = 0; h < NS; ++h)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[u][h][q][e] = 0.f;
+  const __half* qa = Qp + (lane & 7) * qstride + 8 * (lane >> 3);
+#pragma unroll
+  for (int jj = 0; jj < JW; ++jj) {
+    const int j = j0 + jj;
+    uint32_t b[NQ][4];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) ldsm_x4(b[q][0], b[q][1], b[q][2], b[q][3], qa + q * 8 * qstride + 32 * j);
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const uint8_t* kb = sub[u].cb;
+      if (!Q8) {
+        // lane c reads the 16-byte chunks 2c and 2c+1 of its box rows in turn
+        const uint8_t* kr = kb + g * 128 + (((2 * c + (j & 1)) ^ g) << 4) + (j >> 1) * BB;
         const uint4 x = *reinterpret_cast<const uint4*>(kr);
         const uint4 y = *reinterpret_cast<const uint4*>(kr + 8 * 128);
-        float(&sj)[4] = (j & 1) ? s1 : s0;
-        mma16816(sj, x.x, y.x, x.y, y.y, b0, b1);
-        mma16816(sj, x.z, y.z, x.w, y.w, b2, b3);
-      }
-    }
-  } else {
-#pragma unroll 4
-    for (int j = 0; j < kMaxDh / 32; ++j) {
-      if (j < nblk) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(b0, b1, b2, b3, qa + 32 * j);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          float(&sj)[4] = s[u][jj % NS][q];
+          mma16816(sj, x.x, y.x, x.y, y.y, b[q][0], b[q][1]);
+          mma16816(sj, x.z, y.z, x.w, y.w, b[q][2], b[q][3]);
+        }
+      } else {
+        const __half* ks = reinterpret_cast<const __half*>(kb + SL.ks_off);
         const int byte = 32 * j + 8 * c;
         int off;
         if (SWZ) {
@@ -1425,100 +1494,178 @@ __device__ __forceinline__ void attn_chunk(const uint8_t* kb, const uint8_t* vb,
         const uint2 y = *reinterpret_cast<const uint2*>(kb + off + 8 * BW);
         const uint32_t xx = x.x ^ 0x80808080u, xy = x.y ^ 0x80808080u;
         const uint32_t yx = y.x ^ 0x80808080u, yy = y.y ^ 0x80808080u;
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
-        mma16816(t, s8x2_to_h2(xx, 0x4140u), s8x2_to_h2(yx, 0x4140u), s8x2_to_h2(xx, 0x4342u),
-                 s8x2_to_h2(yx, 0x4342u), b0, b1);
-        mma16816(t, s8x2_to_h2(xy, 0x4140u), s8x2_to_h2(yy, 0x4140u), s8x2_to_h2(xy, 0x4342u),
-                 s8x2_to_h2(yy, 0x4342u), b2, b3);
+        const uint32_t a0 = s8x2_to_h2(xx, 0x4140u), a1 = s8x2_to_h2(yx, 0x4140u);
+        const uint32_t a2 = s8x2_to_h2(xx, 0x4342u), a3 = s8x2_to_h2(yx, 0x4342u);
+        const uint32_t a4 = s8x2_to_h2(xy, 0x4140u), a5 = s8x2_to_h2(yy, 0x4140u);
+        const uint32_t a6 = s8x2_to_h2(xy, 0x4342u), a7 = s8x2_to_h2(yy, 0x4342u);
         const float sg = __half2float(ks[g * nblk + j]), sg8 = __half2float(ks[(g + 8) * nblk + j]);
-        float(&sj)[4] = (j & 1) ? s1 : s0;
-        sj[0] = fmaf(sg, t[0], sj[0]);
-        sj[1] = fmaf(sg, t[1], sj[1]);
-        sj[2] = fmaf(sg8, t[2], sj[2]);
-        sj[3] = fmaf(sg8, t[3], sj[3]);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          float t[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816(t, a0, a1, a2, a3, b[q][0], b[q][1]);
+          mma16816(t, a4, a5, a6, a7, b[q][2], b[q][3]);
+          float(&sj)[4] = s[u][jj % NS][q];
+          sj[0] = fmaf(sg, t[0], sj[0]);
+          sj[1] = fmaf(sg, t[1], sj[1]);
+          sj[2] = fmaf(sg8, t[2], sj[2]);
+          sj[3] = fmaf(sg8, t[3], sj[3]);
+        }
       }
     }
   }
-  float sc[4] = {s0[0] + s1[0], s0[1] + s1[1], s0[2] + s1[2], s0[3] + s1[3]};
-  // masks: rows g / g+8 are tokens, columns q0 / q0+1 are query rows
-  const int q0 = nt * 8 + 2 * c;
-  bool v0 = g < nvalid, v1 = v0, v2 = g + 8 < nvalid, v3 = v2;
-  if (causal_grp > 0) {
-    v0 = v0 && g <= q0 / causal_grp;
-    v1 = v1 && g <= (q0 + 1) / causal_grp;
-    v2 = v2 && g + 8 <= q0 / causal_grp;
-    v3 = v3 && g + 8 <= (q0 + 1) / causal_grp;
-  }
-  sc[0] = v0 ? sc[0] : -INFINITY;
-  sc[1] = v1 ? sc[1] : -INFINITY;
-  sc[2] = v2 ? sc[2] : -INFINITY;
-  sc[3] = v3 ? sc[3] : -INFINITY;
-  float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+  if (NS == 2) {
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-  }
-  const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
-  float a0 = 1.f, a1 = 1.f, p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-  if (mn0 != -INFINITY) {
-    a0 = exp2f(st.m[0] - mn0);
-    p0 = exp2f(sc[0] - mn0);
-    p2 = exp2f(sc[2] - mn0);
-  }
-  if (mn1 != -INFINITY) {
-    a1 = exp2f(st.m[1] - mn1);
-    p1 = exp2f(sc[1] - mn1);
-    p3 = exp2f(sc[3] - mn1);
-  }
-  float r0 = p0 + p2, r1 = p1 + p3;
+    for (int q = 0; q < NQ; ++q)
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    r0 += __shfl_xor_sync(0xffffffffu, r0, o);
-    r1 += __shfl_xor_sync(0xffffffffu, r1, o);
+      for (int e = 0; e < 4; ++e) s[0][0][q][e] += s[0][NS - 1][q][e];
   }
-  st.l[0] = fmaf(st.l[0], a0, r0);
-  st.l[1] = fmaf(st.l[1], a1, r1);
-  st.m[0] = mn0;
-  st.m[1] = mn1;
+  // shares to the owners (n-tile q is owned by warp q % wpg)
+  int own = 0;
 #pragma unroll
-  for (int mi = 0; mi < kMaxDh / 16; ++mi) {
-    st.acc[mi][0] *= a0;
-    st.acc[mi][1] *= a1;
-    st.acc[mi][2] *= a0;
-    st.acc[mi][3] *= a1;
+  for (int q = 0; q < NQ; ++q) {
+    if (dp != own) {
+      const int w = dp - (dp > own ? 1 : 0);
+#pragma unroll
+      for (int u = 0; u < NU; ++u)
+        X.s[((w * NU + u) * NQ + q) * 32 + lane] =
+            make_float4(s[u][0][q][0], s[u][0][q][1], s[u][0][q][2], s[u][0][q][3]);
+    }
+    own = own + 1 == wpg ? 0 : own + 1;
   }
-  // O^T += V^T P^T: A = V^T from the V rows (ldmatrix.trans), B = P^T from
-  // the S^T accumulators transposed per 8x8 block
+  group_sync(bar_id, nthr);
+  // the owner's softmax step for each of its n-tiles (one code body: the
+  // tile's scores are first selected into sq)
+  for (int q = dp; q < NQ; q += wpg) {
+    float sq[NU][4];
+#pragma unroll
+    for (int u = 0; u < NU; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = s[u][0][0][e];
+#pragma unroll
+        for (int qq = 1; qq < NQ; ++qq) v = q == qq ? s[u][0][qq][e] : v;
+        sq[u][e] = v;
+      }
+    for (int w = 0; w < wpg - 1; ++w) {
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        const float4 v = X.s[((w * NU + u) * NQ + q) * 32 + lane];
+        sq[u][0] += v.x;
+        sq[u][1] += v.y;
+        sq[u][2] += v.z;
+        sq[u][3] += v.w;
+      }
+    }
+    // masks: rows g / g+8 are tokens, columns q0 / q0+1 are query rows
+    const int q0 = q * 8 + 2 * c;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const int nv = sub[u].nvalid, cg = sub[u].causal;
+      bool v0 = g < nv, v1 = v0, v2 = g + 8 < nv, v3 = v2;
+      if (cg > 0) {
+        v0 = v0 && g <= q0 / cg;
+        v1 = v1 && g <= (q0 + 1) / cg;
+        v2 = v2 && g + 8 <= q0 / cg;
+        v3 = v3 && g + 8 <= (q0 + 1) / cg;
+      }
+      float(&sc)[4] = sq[u];
+      sc[0] = v0 ? sc[0] : -INFINITY;
+      sc[1] = v1 ? sc[1] : -INFINITY;
+      sc[2] = v2 ? sc[2] : -INFINITY;
+      sc[3] = v3 ? sc[3] : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(sc[0], sc[2]));
+      mx1 = fmaxf(mx1, fmaxf(sc[1], sc[3]));
+    }
+    // The reference m of a column moves only when a score passes it by more
+    // than kAttnLazy (p then stays below 2^kAttnLazy): the common step needs
+    // one vote instead of the max reduction, and no rescaling. The result is
+    // the same softmax: O and l are both taken relative to m.
+    float4 ml = X.m[q * 32 + lane];
+    float mn0 = ml.x, mn1 = ml.y, a0 = 1.f, a1 = 1.f;
+    if (__any_sync(0xffffffffu, mx0 > ml.x + kAttnLazy || mx1 > ml.y + kAttnLazy)) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      mn0 = fmaxf(ml.x, mx0);
+      mn1 = fmaxf(ml.y, mx1);
+      a0 = ex2(ml.x - (mn0 == -INFINITY ? 0.f : mn0));
+      a1 = ex2(ml.y - (mn1 == -INFINITY ? 0.f : mn1));
+    }
+    // a column with nothing visible yet keeps m = -inf and p = 0
+    const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+    float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const float p0 = ex2(sq[u][0] - b0), p1 = ex2(sq[u][1] - b1);
+      const float p2 = ex2(sq[u][2] - b0), p3 = ex2(sq[u][3] - b1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      X.p[(q * NU + u) * 32 + lane] = make_uint2(movm_trans(h2u(__floats2half2_rn(p0, p1))),
+                                                 movm_trans(h2u(__floats2half2_rn(p2, p3))));
+    }
+    // l stays this lane's share (its tokens g, g+8); the lanes are added once, at the end
+    ml = make_float4(mn0, mn1, fmaf(ml.z, a0, l0), fmaf(ml.w, a1, l1));
+    X.m[q * 32 + lane] = ml;
+    X.f[q * 32 + lane] = make_float2(a0, a1);
+  }
+  group_sync(bar_id, nthr);
+  // every warp: rescale, then O^T += V^T P^T (A = V^T from the V rows by
+  // ldmatrix.trans, B = the owners' P^T fragments)
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const float2 f = X.f[q * 32 + lane];
+    if (!__any_sync(0xffffffffu, f.x != 1.f || f.y != 1.f)) continue;  // the max held: nothing to rescale
+#pragma unroll
+    for (int mi = 0; mi < 2 * JW; ++mi) {
+      st.acc[q][mi][0] *= f.x;
+      st.acc[q][mi][1] *= f.y;
+      st.acc[q][mi][2] *= f.x;
+      st.acc[q][mi][3] *= f.y;
+    }
+  }
   const int vt = (lane & 7) + 8 * (lane >> 4);  // token row this lane addresses
   const int vsub = (lane >> 3) & 1;
-  const uint8_t* vrow = vb + vt * BW;
-  if (!Q8) {
-    const uint32_t pb0 = movm_trans(h2u(__floats2half2_rn(p0, p1)));
-    const uint32_t pb1 = movm_trans(h2u(__floats2half2_rn(p2, p3)));
-    // tokens 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3) beyond nvalid hold no data
-    const uint32_t mlo = (2 * c < nvalid ? 0xffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
-    const uint32_t mhi = (2 * c + 8 < nvalid ? 0xffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
 #pragma unroll
-    for (int mi = 0; mi < kMaxDh / 16; ++mi) {
-      if (mi < nmt) {
-        const int M = mt0 + mi;  // 16 dims = 32 bytes: box M / 4, chunks 2 (M % 4) + vsub
+  for (int u = 0; u < NU; ++u) {
+    uint2 pb[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) pb[q] = X.p[(q * NU + u) * 32 + lane];
+    const uint8_t* vrow = sub[u].cb + SL.v_off + vt * BW;
+    const int nv = sub[u].nvalid;
+    if (!Q8) {
+      // tokens 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3) beyond nvalid hold no data
+      const uint32_t mlo = (2 * c < nv ? 0xffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
+      const uint32_t mhi = (2 * c + 8 < nv ? 0xffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int mi = 0; mi < 2 * JW; ++mi) {
+        const int M = 2 * j0 + mi;  // 16 dims = 32 bytes: box M / 4, chunks 2 (M % 4) + vsub
         const uint8_t* addr = vrow + (M >> 2) * BB + (((2 * (M & 3) + vsub) ^ (lane & 7)) << 4);
         uint32_t x0, x1, x2, x3;
         ldsm_x4_trans(x0, x1, x2, x3, addr);
-        mma16816(st.acc[mi], x0 & mlo, x1 & mlo, x2 & mhi, x3 & mhi, pb0, pb1);
-      }
-    }
-  } else {
-    // V = scale[token][block] x code: the scale goes into P^T per block
+        x0 &= mlo;
+        x1 &= mlo;
+        x2 &= mhi;
+        x3 &= mhi;
 #pragma unroll
-    for (int jb = 0; jb < kMaxDh / 32; ++jb) {
-      if (2 * jb < nmt) {
-        const int blk = mt0 / 2 + jb;
-        const float sg = g < nvalid ? __half2float(vs[g * nblk + blk]) : 0.f;
-        const float sg8 = g + 8 < nvalid ? __half2float(vs[(g + 8) * nblk + blk]) : 0.f;
-        const uint32_t pb0 = movm_trans(h2u(__floats2half2_rn(p0 * sg, p1 * sg)));
-        const uint32_t pb1 = movm_trans(h2u(__floats2half2_rn(p2 * sg8, p3 * sg8)));
+        for (int q = 0; q < NQ; ++q) mma16816(st.acc[q][mi], x0, x1, x2, x3, pb[q].x, pb[q].y);
+      }
+    } else {
+      // V = scale[token][block] x code, formed in binary16: the exact integer
+      // code times the block scale of each of the lane's tokens 2c, 2c+1
+      // (fragment registers 0, 1) and 2c+8, 2c+9 (registers 2, 3); tokens
+      // beyond nvalid get scale 0
+      const __half* vs = reinterpret_cast<const __half*>(sub[u].cb + SL.vs_off);
+#pragma unroll
+      for (int jb = 0; jb < JW; ++jb) {
+        const int blk = j0 + jb;
+        const __half z = __ushort_as_half(0);
+        const __half2 s01 = __halves2half2(2 * c < nv ? vs[(2 * c) * nblk + blk] : z,
+                                           2 * c + 1 < nv ? vs[(2 * c + 1) * nblk + blk] : z);
+        const __half2 s89 = __halves2half2(2 * c + 8 < nv ? vs[(2 * c + 8) * nblk + blk] : z,
+                                           2 * c + 9 < nv ? vs[(2 * c + 9) * nblk + blk] : z);
         const uint8_t* addr = SWZ ? vrow + (blk >> 2) * BB + (((2 * (blk & 3) + vsub) ^ (lane & 7)) << 4)
                                   : vrow + 32 * blk + 16 * vsub;
         uint32_t r0_, r1_, r2_, r3_;
@@ -1527,11 +1674,20 @@ __device__ __forceinline__ void attn_chunk(const uint8_t* kb, const uint8_t* vb,
         r1_ ^= 0x80808080u;
         r2_ ^= 0x80808080u;
         r3_ ^= 0x80808080u;
+        auto sc = [](uint32_t v, __half2 m) {
+          const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&v), m);
+          return h2u(h);
+        };
         // m-rows g / g+8 of a tile are the block's even / odd dims
-        mma16816(st.acc[2 * jb], s8x2_to_h2(r0_, 0x4240u), s8x2_to_h2(r0_, 0x4341u), s8x2_to_h2(r2_, 0x4240u),
-                 s8x2_to_h2(r2_, 0x4341u), pb0, pb1);
-        mma16816(st.acc[2 * jb + 1], s8x2_to_h2(r1_, 0x4240u), s8x2_to_h2(r1_, 0x4341u),
-                 s8x2_to_h2(r3_, 0x4240u), s8x2_to_h2(r3_, 0x4341u), pb0, pb1);
+        const uint32_t e0 = sc(s8x2_to_h2(r0_, 0x4240u), s01), e1 = sc(s8x2_to_h2(r0_, 0x4341u), s01);
+        const uint32_t e2 = sc(s8x2_to_h2(r2_, 0x4240u), s89), e3 = sc(s8x2_to_h2(r2_, 0x4341u), s89);
+        const uint32_t o0 = sc(s8x2_to_h2(r1_, 0x4240u), s01), o1 = sc(s8x2_to_h2(r1_, 0x4341u), s01);
+        const uint32_t o2 = sc(s8x2_to_h2(r3_, 0x4240u), s89), o3 = sc(s8x2_to_h2(r3_, 0x4341u), s89);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          mma16816(st.acc[q][2 * jb], e0, e1, e2, e3, pb[q].x, pb[q].y);
+          mma16816(st.acc[q][2 * jb + 1], o0, o1, o2, o3, pb[q].x, pb[q].y);
+        }
       }
     }
   }
@@ -1602,13 +1758,9 @@ __device__ void attn_load_kv(const ModelDesc& md, int fa_i, int page, int kh, in
   }
 }
 
-// Shared memory of the attention phase, inside the phase region.
-constexpr int kAttnQBytes = (kMaxQRows * (kMaxDh + 8) * 2 + 255) / 256 * 256;
-constexpr int kAttnNewBytes = 16384;                          // largest slot (fp16, dh 256)
-constexpr int kAttnMergeBytes = 4 * (4 + 4 * (kMaxDh / 16)) * 32 * 4;  // worst plan: 1 x 4 warps, 16 m-tiles
-static_assert(kAttnQBytes + kAttnNewBytes + kAttnMergeBytes + 16 <= kPhaseBytes, "attention shared memory");
-static_assert((2 * kMaxQRows * kMaxSplits + kMaxQRows) * 4 <= kAttnQBytes + kAttnNewBytes + kAttnMergeBytes,
-              "attention combine scratch (below the phase's flag word)");
+static_assert(attn_qbytes(kMaxQRows / 8, kMaxDh) + 16384 + 16 <= kPhaseBytes, "attention shared memory");
+// the merge's weights (2 x rows x partials + rows floats) stay below the
+// phase's flag word: the host keeps rows x partials within kAttnCombineFloats
 static_assert(kAttnBarOff + 2 * kAttnMaxSlots * 8 <= kMiscBytes, "attention mbarriers");
 
 // Every block of a (sequence, kv head) merges its share of the splits'
@@ -1618,24 +1770,27 @@ static_assert(kAttnBarOff + 2 * kAttnMaxSlots * 8 <= kMiscBytes, "attention mbar
 // row the weights 2^(m_s - M) and 1/sum(l_s w_s); then groups of 4 threads sum
 // one output float4 over the splits (each thread a quarter of them, all its
 // loads in flight) and a shuffle adds the four.
-__device__ __noinline__ void attn_combine(const ModelDesc& md, const StepDesc& sd, int si, int kh, int nsplit,
-                                          int qrows, int row0, int j, float* wsm) {
+__device__ __noinline__ void attn_combine(const ModelDesc& md, const StepDesc& sd, int si, int kh, int nblocks,
+                                          int ngroups, int qrows, int row0, int j, float* wsm) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int dh = md.dh, grp = md.hq / md.hkv;
-  const int item0 = sd.seq_item0[si] + kh * nsplit;
+  const int item0 = sd.seq_item0[si] + kh * nblocks;
+  const int nsplit = nblocks * ngroups;  // partials: every group of every split block
   const int n = qrows * nsplit;
   float* wm = wsm;          // [qrows][nsplit]: m, then the weight
   float* wl = wsm + n;      // [qrows][nsplit]: l
   float* inv = wsm + 2 * n;  // [qrows]
   auto part = [&](int sp, int r) {
-    return md.attn_part + (static_cast<size_t>(item0 + sp) * kMaxQRows + r) * kPartStride;
+    return md.attn_part +
+           ((static_cast<size_t>(item0 + sp / ngroups) * kMaxAttnGroups + sp % ngroups) * md.part_rows + r) *
+               md.part_stride;
   };
   for (int base = 0; base < n; base += kThreads * 8) {
     float2 ml[8];
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       const int idx = base + b * kThreads + tid;
-      ml[b] = idx < n ? __ldcg(reinterpret_cast<const float2*>(part(idx % nsplit, idx / nsplit) + kMaxDh))
+      ml[b] = idx < n ? __ldcg(reinterpret_cast<const float2*>(part(idx % nsplit, idx / nsplit) + dh))
                       : make_float2(0.f, 0.f);
     }
 #pragma unroll
@@ -1668,8 +1823,8 @@ __device__ __noinline__ void attn_combine(const ModelDesc& md, const StepDesc& s
   constexpr int kSlots = kThreads / kG;     // outputs per pass of the block
   const int q = tid & (kG - 1), slot = tid / kG;
   // the pass loop is warp-uniform (the shuffles below need the whole warp)
-  for (int pass = 0; j + nsplit * (warp * (32 / kG) + kSlots * pass) < total; ++pass) {
-    const int o = j + nsplit * (slot + kSlots * pass);
+  for (int pass = 0; j + nblocks * (warp * (32 / kG) + kSlots * pass) < total; ++pass) {
+    const int o = j + nblocks * (slot + kSlots * pass);
     const bool valid = o < total;
     const int r = valid ? o / d4n : 0, d4 = valid ? o - r * d4n : 0;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1735,7 +1890,7 @@ __device__ bool attn_splits_ready(const ModelDesc& md, const StepDesc& sd, int k
 // angles from mtp_rope; the new-rows chunk holds the slots 0..k-1 that earlier
 // phases of this launch stored (read back) and the row's own K/V at slot k,
 // all visible to it.
-template <bool Q8, bool SWZ>
+template <bool Q8, bool SWZ, int NQ, int JW>
 __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const Smem& sm,
                                         float* scratch_row, WarpCtx& wc, int mp) {
   const LayerDesc& L = md.layer[layer];
@@ -1745,20 +1900,23 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
   const int g = lane >> 2, c = lane & 3;
   const AttnSlot SL = attn_slot_layout(dh, Q8 ? 1 : 0);
   const AttnBuf ab = attn_buf(sm);
-  const int ng = sd.attn_ng, wpg = sd.attn_wpg, dsplit = sd.attn_dsplit, spg = sd.attn_spg;
-  const int tg = warp / wpg, wi = warp % wpg;
+  // a group of wpg warps takes one chunk at a time; each of its warps owns
+  // every query n-tile and the dims of JW 32-dim blocks
+  const int ng = sd.attn_ng, wpg = sd.attn_wpg, spg = sd.attn_spg;
+  const int tg = warp / wpg, dp = warp % wpg;
   const bool in_group = tg < ng;
-  const int nt = wi / dsplit, dp = wi % dsplit;
-  const int nmt = (dh / 16) / dsplit, mt0 = dp * nmt;
+  const int j0 = dp * JW;
+  const int nmt = 2 * JW, mt0 = 2 * j0;
   const int qstride = dh + 8;
   __half* Qp = reinterpret_cast<__half*>(sm.phase());
-  uint8_t* newt = sm.phase() + kAttnQBytes;
-  float* mbuf = reinterpret_cast<float*>(sm.phase() + kAttnQBytes + kAttnNewBytes);
-  int* flag = reinterpret_cast<int*>(sm.phase() + kAttnQBytes + kAttnNewBytes + kAttnMergeBytes);
+  uint8_t* newt = sm.phase() + attn_qbytes(NQ, dh);
+  // this group's exchange area
+  constexpr int NU = attn_nu(NQ, Q8 ? 1 : 0);
+  const AttnX<NQ, NU> X(sm.phase() + attn_xoff(NQ, dh, Q8 ? 1 : 0) + tg * attn_xslab(wpg, NQ, Q8 ? 1 : 0), wpg);
+  int* flag = reinterpret_cast<int*>(sm.phase() + kPhaseBytes - 16);
   const float q_scale = 1.4426950408889634f / sqrtf(static_cast<float>(dh));  // log2(e) / sqrt(dh)
   const int kq_off = 2 * md.hq * dh;    // k after q and gate
   const int vq_off = kq_off + hkv * dh;  // v after k
-  const int mstride = 4 + 4 * nmt;      // floats per lane of one warp's merge record
   bool ok = true;
 
   for (int item = blockIdx.x; item < sd.n_attn_items; item += gridDim.x) {
@@ -1773,7 +1931,7 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
     // present them; rows past qrows are zero
     // batches of 4 pairs per thread: all of a batch's loads are issued before
     // its shared-memory stores
-    const int nqe = nq * 8 * (dh / 2);
+    const int nqe = NQ * 8 * (dh / 2);  // every n-tile of the variant: rows past qrows are zero
     for (int base = 0; base < nqe; base += kThreads * 4) {
       float qa[4][2], qb[4][2];
       float2 qc[4][2];
@@ -1853,117 +2011,113 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
     }
     math_sync();
 
-    AttnState st;
-    st.m[0] = st.m[1] = -INFINITY;
-    st.l[0] = st.l[1] = 0.f;
+    AttnAcc<NQ, 2 * JW> st;
 #pragma unroll
-    for (int mi = 0; mi < kMaxDh / 16; ++mi)
+    for (int q = 0; q < NQ; ++q) {
+      if (in_group && q % wpg == dp) X.m[q * 32 + lane] = make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) st.acc[mi][e] = 0.f;
-    const bool active = in_group && nt < nq;
+      for (int mi = 0; mi < 2 * JW; ++mi)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.acc[q][mi][e] = 0.f;
+    }
     // this block's chunks round-robin over the groups; the step's own rows
-    // (last split) are one more chunk, read from the new-rows tile
+    // (last split) are one more chunk, read from the new-rows tile. Every warp
+    // of a group runs every chunk (also after a failed wait: its result is
+    // then void) so that the group's barriers always meet.
     if (in_group) {
       const int nv = it.nch + (last ? 1 : 0);
-      for (int i = tg; i < nv; i += ng) {
-        const bool cached = i < it.nch;
-        const int slot = tg * spg + static_cast<int>(wc.kv_pos % static_cast<uint32_t>(spg));
-        const uint8_t* cb = newt;
-        int nvalid = n_new, causal = mp ? 0 : grp;
-        if (cached) {
-          if (ok)
-            ok = mbar_wait_bounded(ab.full + slot, (wc.kv_pos / spg) & 1u, md, sd.barrier_timeout_ns,
-                                   DEV_COPY_TIMEOUT);
-          cb = ab.slots + slot * SL.bytes;
-          nvalid = min(kChunk, Lc - (it.cb + i) * kChunk);
-          causal = 0;
+      for (int i = tg; i < nv; i += NU * ng) {
+        // chunks i, i + ng, ... (NU of them, those past nv void): cached pages
+        // come from the group's slots in order, the step's own rows from newt
+        AttnSub sub[NU];
+        int slot[NU];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+          const int iu = i + u * ng;
+          slot[u] = -1;
+          sub[u] = AttnSub{newt, 0, 0};
+          if (iu < it.nch) {
+            const uint32_t pos = wc.kv_pos + u;
+            slot[u] = tg * spg + static_cast<int>(pos % static_cast<uint32_t>(spg));
+            if (ok)
+              ok = mbar_wait_bounded(ab.full + slot[u], (pos / spg) & 1u, md, sd.barrier_timeout_ns,
+                                     DEV_COPY_TIMEOUT);
+            sub[u] = AttnSub{ab.slots + slot[u] * SL.bytes, min(kChunk, Lc - (it.cb + iu) * kChunk), 0};
+          } else if (iu < nv) {
+            sub[u] = AttnSub{newt, n_new, mp ? 0 : grp};
+          }
         }
-        if (ok && active)
-          attn_chunk<Q8, SWZ>(cb, cb + SL.v_off, reinterpret_cast<const __half*>(cb + SL.ks_off),
-                              reinterpret_cast<const __half*>(cb + SL.vs_off), Qp, qstride, dh, nt, mt0, nmt, nvalid,
-                              causal, lane, st);
-        if (cached) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ab.empty + slot);
-          ++wc.kv_pos;
-        }
+        attn_chunk<Q8, SWZ, NQ, JW, NU>(sub, SL, Qp, qstride, dh, j0, lane, wpg, dp, X, 2 + tg, st);
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+          if (slot[u] >= 0) {
+            if (lane == 0) mbar_arrive(ab.empty + slot[u]);
+            ++wc.kv_pos;
+          }
       }
     }
 
-    // merge the groups into group 0, in group order
-    if (ng > 1) {
-      if (in_group && tg > 0) {
-        float* pb = mbuf + ((tg - 1) * wpg + wi) * mstride * 32 + lane;
-        pb[0] = st.m[0];
-        pb[32] = st.m[1];
-        pb[64] = st.l[0];
-        pb[96] = st.l[1];
+    // write out: directly if this block's one group holds the whole head,
+    // else this group's partial (unnormalised O, m, l) for the merge
+    const bool merged = it.nsplit > 1 || ng > 1;
+    float* part = md.attn_part + (static_cast<size_t>(item) * kMaxAttnGroups + tg) * md.part_rows * md.part_stride;
+    if (in_group) {
+      // the owners' sums (lanes added) for every warp of the group; the owners
+      // also write m and l of a partial
 #pragma unroll
-        for (int mi = 0; mi < kMaxDh / 16; ++mi)
-          if (mi < nmt)
+      for (int q = 0; q < NQ; ++q) {
+        if (q % wpg == dp) {
+          const float4 ml = X.m[q * 32 + lane];
+          float lq[2] = {ml.z, ml.w};
+          const float mq[2] = {ml.x, ml.y};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) pb[(4 + 4 * mi + e) * 32] = st.acc[mi][e];
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) lq[e] += __shfl_xor_sync(0xffffffffu, lq[e], o);
+          if (g == 0) X.l[q * 4 + c] = make_float2(lq[0], lq[1]);
+          if (merged && g == 0) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int qr = q * 8 + 2 * c + e;
+              if (qr < qrows) {
+                __stcg(part + static_cast<size_t>(qr) * md.part_stride + dh, mq[e]);
+                __stcg(part + static_cast<size_t>(qr) * md.part_stride + dh + 1, lq[e]);
+              }
+            }
+          }
+        }
       }
-      math_sync();
-      if (in_group && tg == 0) {
-        for (int g2 = 1; g2 < ng; ++g2) {
-          const float* pb = mbuf + ((g2 - 1) * wpg + wi) * mstride * 32 + lane;
-          float fa[2], fb[2];
+      group_sync(2 + tg, wpg * 32);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (q < nq) {
+          const float2 lq = X.l[q * 4 + c];
+          // this lane's two query columns of n-tile q: destination row and scale
+          float* dst[2];
+          float sc[2];
+          bool okq[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float mo = pb[32 * e], lo = pb[64 + 32 * e];
-            const float M = fmaxf(st.m[e], mo);
-            fa[e] = st.m[e] == -INFINITY ? 0.f : exp2f(st.m[e] - M);
-            fb[e] = mo == -INFINITY ? 0.f : exp2f(mo - M);
-            st.l[e] = st.l[e] * fa[e] + lo * fb[e];
-            st.m[e] = M;
+            const int qr = q * 8 + 2 * c + e;
+            okq[e] = qr < qrows;
+            const int t = qr / grp, hh = kh * grp + qr % grp;
+            dst[e] = !merged ? md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh
+                             : part + static_cast<size_t>(qr) * md.part_stride;
+            sc[e] = !merged ? 1.0f / (e ? lq.y : lq.x) : 1.0f;
           }
 #pragma unroll
-          for (int mi = 0; mi < kMaxDh / 16; ++mi)
+          for (int mi = 0; mi < 2 * JW; ++mi)
             if (mi < nmt)
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                st.acc[mi][e] = st.acc[mi][e] * fa[e & 1] + pb[(4 + 4 * mi + e) * 32] * fb[e & 1];
-        }
-      }
-      math_sync();
-    }
-
-    // write out: directly if one split, else a partial for the combine
-    float* part = md.attn_part + static_cast<size_t>(item) * kMaxQRows * kPartStride;
-    if (in_group && tg == 0 && active) {
-      // this lane's two query columns: destination row and scale
-      float* dst[2];
-      float sc[2];
-      bool okq[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int qr = nt * 8 + 2 * c + e;
-        okq[e] = qr < qrows;
-        const int t = qr / grp, hh = kh * grp + qr % grp;
-        dst[e] = it.nsplit == 1 ? md.o + static_cast<size_t>(row0 + t) * md.o_stride + hh * dh
-                                : part + qr * kPartStride;
-        sc[e] = it.nsplit == 1 ? 1.0f / st.l[e] : 1.0f;
-      }
-#pragma unroll
-      for (int mi = 0; mi < kMaxDh / 16; ++mi)
-        if (mi < nmt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (okq[e & 1]) __stcg(dst[e & 1] + attn_dim<Q8>(mt0 + mi, e < 2 ? g : g + 8), st.acc[mi][e] * sc[e & 1]);
-      if (it.nsplit > 1 && dp == 0 && g == 0) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int qr = nt * 8 + 2 * c + e;
-          if (qr < qrows) {
-            __stcg(part + qr * kPartStride + kMaxDh, st.m[e]);
-            __stcg(part + qr * kPartStride + kMaxDh + 1, st.l[e]);
-          }
+                if (okq[e & 1])
+                  __stcg(dst[e & 1] + attn_dim<Q8>(mt0 + mi, e < 2 ? g : g + 8), st.acc[q][mi][e] * sc[e & 1]);
         }
       }
     }
-    if (it.nsplit > 1) {
-      // announce this split's partial, wait for the others, merge this split's share
+    if (merged) {
+      // announce this block's partials, wait for the others, merge this block's share
       __threadfence();
       math_sync();
       if (tid == 0) {
@@ -1972,12 +2126,29 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
         *flag = attn_splits_ready(md, sd, key, fa_i + mp, it.nsplit) ? 1 : 0;
       }
       math_sync();
-      if (*flag) attn_combine(md, sd, si, kh, it.nsplit, qrows, row0, it.j, reinterpret_cast<float*>(sm.phase()));
+      if (*flag) attn_combine(md, sd, si, kh, it.nsplit, ng, qrows, row0, it.j, reinterpret_cast<float*>(sm.phase()));
       else ok = false;
     }
     math_sync();
   }
   return ok;
+}
+
+// The attention variant for the step's query n-tiles per (sequence, kv head)
+// and 32-dim blocks per warp: each warp holds nq n-tiles x 2 jw m-tiles of O^T.
+template <bool Q8, bool SWZ>
+__device__ __forceinline__ bool attn_dispatch(int nq, int jw, const ModelDesc& md, const StepDesc& sd, int layer,
+                                              const Smem& sm, float* scratch_row, WarpCtx& wc, int mp) {
+  switch (nq) {
+    case 1:
+      if (jw == 4) return attn_phase<Q8, SWZ, 1, 4>(md, sd, layer, sm, scratch_row, wc, mp);
+      return attn_phase<Q8, SWZ, 1, 2>(md, sd, layer, sm, scratch_row, wc, mp);
+    case 2: return attn_phase<Q8, SWZ, 2, 2>(md, sd, layer, sm, scratch_row, wc, mp);
+    case 3: return attn_phase<Q8, SWZ, 3, 2>(md, sd, layer, sm, scratch_row, wc, mp);
+    case 4: return attn_phase<Q8, SWZ, 4, 1>(md, sd, layer, sm, scratch_row, wc, mp);
+    case 5: return attn_phase<Q8, SWZ, 5, 1>(md, sd, layer, sm, scratch_row, wc, mp);
+    default: return attn_phase<Q8, SWZ, 6, 1>(md, sd, layer, sm, scratch_row, wc, mp);
+  }
 }
 
 static_assert(kWarps * (2 * kMaxT * 128 + kMaxT * 10) * 4 <= kPhaseBytes, "Gated DeltaNet shared memory");
@@ -2344,9 +2515,10 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
   const int n_main = 1 + 5 * md.n_layers + 2;
   const int n_phases = n_main + (md.has_mtp ? 9 * md.n_draft : 0);
   auto attention = [&](int layer, int mp) {
-    if (!md.kv_q8) return attn_phase<false, true>(md, sd, layer, sm, my_scratch, wc, mp);
-    if (md.dh % 128 == 0) return attn_phase<true, true>(md, sd, layer, sm, my_scratch, wc, mp);
-    return attn_phase<true, false>(md, sd, layer, sm, my_scratch, wc, mp);
+    if (!md.kv_q8) return attn_dispatch<false, true>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, my_scratch, wc, mp);
+    if (md.dh % 128 == 0)
+      return attn_dispatch<true, true>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, my_scratch, wc, mp);
+    return attn_dispatch<true, false>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, my_scratch, wc, mp);
   };
   if (md.dbg_time && blockIdx.x == 0 && threadIdx.x == 0) md.dbg_time[0] = globaltimer();
   for (int ph = 0; ph < n_phases; ++ph) {
