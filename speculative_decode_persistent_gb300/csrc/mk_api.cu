@@ -19,7 +19,7 @@
 
 namespace mk {
 cudaError_t pack_units(const PackSrc& p, uint8_t* dst, int n_tiles, int nsb, cudaStream_t s);
-cudaError_t launch_persistent(const ModelDesc* md, const StepDesc* sd, float* attn_scratch, int grid,
+cudaError_t launch_persistent(const ModelDesc* md, const StepDesc* sd, int grid,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, cudaStream_t stream);
 cudaError_t configure_persistent(int* blocks_per_sm);
 }  // namespace mk
@@ -179,7 +179,6 @@ struct mk_ctx {
   StepDesc* sd_host = nullptr;  // pinned
   int32_t* out_host = nullptr;  // pinned [kOutInts + 4]
   int32_t* pt_host = nullptr;   // pinned page-table mirror
-  float* attn_scratch = nullptr;
   double* inv_freq = nullptr;  // device [kMaxDh/2]
   CUtensorMap tm_k{}, tm_v{};  // 2-D tensor maps of the K and V pools (attention page copies)
   std::vector<void*> allocs;
@@ -591,7 +590,6 @@ mk_status mk_create(const mk_layout* layout, const mk_weights* w, const mk_buffe
       (dev_alloc(c, &md.out, kOutInts * 4)) ||
       (dev_alloc(c, &md.bar, 64)) ||
       (dev_alloc(c, &md.err, 64)) ||
-      (dev_alloc(c, &c->attn_scratch, nrec * 2 * kMaxDh * 4)) ||
       (dev_alloc(c, &md.mtp_in, L.has_mtp ? static_cast<size_t>(kMaxRows) * 2 * H * 4 : 0)) ||
       (dev_alloc(c, &md.mtp_h, L.has_mtp ? static_cast<size_t>(kMaxSeqs) * H * 4 : 0)) ||
       (dev_alloc(c, &md.mtp_rope, static_cast<size_t>(kMaxSeqs) * (kMaxDh / 2) * sizeof(float2))) ||
@@ -914,7 +912,7 @@ mk_status mk_step_launch(mk_ctx* c) {
     return MK_ERR_CUDA;
   cudaEventRecord(c->ev0, c->stream);
   const cudaError_t e =
-      launch_persistent(c->md_dev, c->sd_dev, c->attn_scratch, c->grid, &c->tm_k, &c->tm_v, c->stream);
+      launch_persistent(c->md_dev, c->sd_dev, c->grid, &c->tm_k, &c->tm_v, c->stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? MK_ERR_LAUNCH : MK_ERR_CUDA;
@@ -992,7 +990,7 @@ void* g_static_addr[kMaxDevices] = {nullptr};
 
 struct StaticLayout {
   size_t md, x, yin, o, h, gu, logits, tickets, attn_part, attn_tickets, norm_part, top_val, top_idx, out, bar, err,
-      attn_scratch, total;
+      total;
 };
 
 StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
@@ -1017,7 +1015,6 @@ StaticLayout static_layout(const mk_ctx* c, int n_attn_items) {
   take(L.out, kOutInts * 4);
   take(L.bar, 64);
   take(L.err, 64);
-  take(L.attn_scratch, nrec * 2 * kMaxDh * 4);
   L.total = at;
   return L;
 }
@@ -1065,7 +1062,6 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
   md.bar = reinterpret_cast<uint32_t*>(base + SL.bar);
   md.err = reinterpret_cast<int32_t*>(base + SL.err);
   ModelDesc* md_dev = reinterpret_cast<ModelDesc*>(base + SL.md);
-  float* attn_scratch = reinterpret_cast<float*>(base + SL.attn_scratch);
   // The array keeps the previous call's contents: clear what must start at zero.
   if (cudaMemcpyAsync(md_dev, &md, sizeof(ModelDesc), cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
       cudaMemsetAsync(md.tickets, 0, c->tickets_bytes, c->stream) != cudaSuccess ||
@@ -1076,7 +1072,7 @@ extern "C" mk_status mk_step_static(mk_ctx* c, int32_t n_rows, const int32_t* to
     return MK_ERR_CUDA;
   c->h2d_bytes += sizeof(ModelDesc);
   cudaEventRecord(c->ev0, c->stream);
-  const cudaError_t e = launch_persistent(md_dev, c->sd_dev, attn_scratch, c->grid, &c->tm_k, &c->tm_v, c->stream);
+  const cudaError_t e = launch_persistent(md_dev, c->sd_dev, c->grid, &c->tm_k, &c->tm_v, c->stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? MK_ERR_LAUNCH : MK_ERR_CUDA;

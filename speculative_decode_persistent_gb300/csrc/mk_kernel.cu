@@ -1700,38 +1700,102 @@ __device__ __forceinline__ int attn_dim(int M, int row) {
   return (M >> 1) * 32 + (M & 1) * 16 + (row < 8 ? 2 * row : 2 * (row - 8) + 1);
 }
 
-// One row of the step's own K or V: rounded (fp16 pool) or quantised (q8
-// pool) into the pool, and the same stored values into the new-rows chunk.
-__device__ void attn_store_kv(const ModelDesc& md, int fa_i, int page, int kh, int slot, const float* x, int which,
-                              uint8_t* tile, __half* tile_scales, const AttnSlot& SL, int t, int lane) {
-  const int dh = md.dh;
+// binary16 nearest to amax / 127 (ties to even), in single precision only: a
+// candidate from the single-precision quotient, then the midpoints to its
+// neighbours compared exactly (127 x a midpoint of two binary16 values has at
+// most 19 significant bits). amax >= 0.
+__device__ __forceinline__ __half q8_block_scale(float amax) {
+  const __half h = __float2half_rn(amax / 127.0f);
+  const unsigned short u = __half_as_ushort(h);
+  const float hf = __half2float(h);
+  if (u < 0x7bffu) {  // the next binary16 up is finite
+    const float up = __half2float(__ushort_as_half(static_cast<unsigned short>(u + 1)));
+    const float pm = 127.0f * (0.5f * (hf + up));
+    if (amax > pm || (amax == pm && (u & 1u))) return __ushort_as_half(static_cast<unsigned short>(u + 1));
+  }
+  if (u > 0 && u < 0x7c00u) {
+    const float dn = __half2float(__ushort_as_half(static_cast<unsigned short>(u - 1)));
+    const float pm = 127.0f * (0.5f * (dn + hf));
+    if (amax < pm || (amax == pm && (u & 1u))) return __ushort_as_half(static_cast<unsigned short>(u - 1));
+  }
+  return h;
+}
+
+// round-half-even of val / d, clamped to [-127, 127] (0 when d = 0), exactly:
+// the single-precision quotient rounded, then corrected by the exact remainder
+// val - q d (q d has at most 18 significant bits)
+__device__ __forceinline__ int q8_code(float val, float d) {
+  if (d == 0.f) return 0;
+  float q = rintf(val / d);
+  const float r = fmaf(-q, d, val), h = 0.5f * d;
+  const bool odd = (static_cast<int>(q) & 1) != 0;
+  if (r > h || (r == h && odd)) q += 1.f;
+  else if (r < -h || (r == -h && odd)) q -= 1.f;
+  return static_cast<int>(fminf(fmaxf(q, -127.f), 127.f));
+}
+
+// K (with RoPE) and V of the step's own row t for kv head kh, from the input
+// projection's output (kr, vr; rope: the row's (cos, sin) per pair), rounded
+// (fp16 pool) or quantised (q8 pool: per 32-dim block, scale = binary16 of
+// amax / 127, code = round(x / scale)) into the pool at (page, slot) and, as
+// stored, into row t of the new-rows chunk. Lane l holds the dims l + 32 j of
+// each half of the row: RoPE pairs dim d < dh/2 with d + dh/2 in the same lane.
+__device__ __noinline__ void attn_new_row(const ModelDesc& md, const float* kr, const float* vr, const float2* rope,
+                                          int fa_i, int page, int kh, int slot, uint8_t* newt, const AttnSlot& SL,
+                                          int t, int lane) {
+  constexpr int kH = kMaxDh / 64;  // 32-dim blocks per half row, at most
+  const int dh = md.dh, nh = dh / 64;
+  const bool q8 = md.kv_q8 != 0;
   const size_t row = ((static_cast<size_t>(fa_i) * md.n_pages + page) * md.hkv + kh) * md.page_tokens + slot;
-  if (!md.kv_q8) {
-    __half* dst = reinterpret_cast<__half*>(which ? md.kv_v : md.kv_k) + row * dh;
-    for (int d = lane; d < dh; d += 32) {
-      const __half hv = __float2half_rn(x[d]);
-      dst[d] = hv;
-      *reinterpret_cast<__half*>(tile + kv_off(SL, t, 2 * d)) = hv;
-    }
-  } else {
-    int8_t* codes = reinterpret_cast<int8_t*>(which ? md.kv_v : md.kv_k) + row * dh;
-    uint16_t* scales = (which ? md.kv_vs : md.kv_ks) + row * (dh / 32);
-    for (int b = 0; b < dh / 32; ++b) {
-      const float val = x[32 * b + lane];
-      const float amax = warp_max(fabsf(val));
-      const __half d16 = __double2half(static_cast<double>(amax) / 127.0);
-      const double dd = static_cast<double>(__half2float(d16));
-      int q = 0;
-      if (dd != 0.0) {
-        double qq = rint(static_cast<double>(val) / dd);
-        qq = qq < -127.0 ? -127.0 : (qq > 127.0 ? 127.0 : qq);
-        q = static_cast<int>(qq);
+#pragma unroll 1
+  for (int w = 0; w < 2; ++w) {
+    float x[2 * kH];  // [half * kH + j]
+#pragma unroll
+    for (int j = 0; j < kH; ++j)
+      if (j < nh) {
+        const int d = 32 * j + lane;
+        if (w == 0) {
+          const float a = __ldcg(kr + d), b = __ldcg(kr + d + dh / 2);
+          const float2 cs = __ldcg(rope + d);
+          x[j] = a * cs.x - b * cs.y;
+          x[kH + j] = a * cs.y + b * cs.x;
+        } else {
+          x[j] = __ldcg(vr + d);
+          x[kH + j] = __ldcg(vr + d + dh / 2);
+        }
       }
-      codes[32 * b + lane] = static_cast<int8_t>(q);
-      tile[kv_off(SL, t, 32 * b + lane)] = static_cast<uint8_t>(static_cast<int8_t>(q));
-      if (lane == 0) {
-        scales[b] = __half_as_ushort(d16);
-        tile_scales[t * (dh / 32) + b] = d16;
+    uint8_t* tile = newt + (w ? SL.v_off : 0);
+    void* pool = w ? md.kv_v : md.kv_k;
+    if (!q8) {
+      __half* dst = reinterpret_cast<__half*>(pool) + row * dh;
+#pragma unroll
+      for (int i = 0; i < 2 * kH; ++i) {
+        const int hf = i / kH, j = i % kH;
+        if (j < nh) {
+          const int d = 32 * (hf * nh + j) + lane;
+          const __half hv = __float2half_rn(x[i]);
+          dst[d] = hv;
+          *reinterpret_cast<__half*>(tile + kv_off(SL, t, 2 * d)) = hv;
+        }
+      }
+    } else {
+      int8_t* codes = reinterpret_cast<int8_t*>(pool) + row * dh;
+      uint16_t* scales = (w ? md.kv_vs : md.kv_ks) + row * (dh / 32);
+      __half* tscale = reinterpret_cast<__half*>(newt + (w ? SL.vs_off : SL.ks_off)) + t * (dh / 32);
+#pragma unroll
+      for (int i = 0; i < 2 * kH; ++i) {
+        const int hf = i / kH, j = i % kH;
+        if (j < nh) {
+          const int blk = hf * nh + j, d = 32 * blk + lane;
+          const __half d16 = q8_block_scale(warp_max(fabsf(x[i])));
+          const int q = q8_code(x[i], __half2float(d16));
+          codes[d] = static_cast<int8_t>(q);
+          tile[kv_off(SL, t, d)] = static_cast<uint8_t>(static_cast<int8_t>(q));
+          if (lane == 0) {
+            scales[blk] = __half_as_ushort(d16);
+            tscale[blk] = d16;
+          }
+        }
       }
     }
   }
@@ -1892,7 +1956,7 @@ __device__ bool attn_splits_ready(const ModelDesc& md, const StepDesc& sd, int k
 // all visible to it.
 template <bool Q8, bool SWZ, int NQ, int JW>
 __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd, int layer, const Smem& sm,
-                                        float* scratch_row, WarpCtx& wc, int mp) {
+                                        WarpCtx& wc, int mp) {
   const LayerDesc& L = md.layer[layer];
   const int fa_i = L.fa_i;
   const int dh = md.dh, hkv = md.hkv, grp = md.hq / md.hkv;
@@ -1992,21 +2056,8 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
         const int row = row0 + (mp ? 0 : t);
         const float* kr = md.yin + static_cast<size_t>(row) * md.n_in_max + kq_off + kh * dh;
         const float* vr = md.yin + static_cast<size_t>(row) * md.n_in_max + vq_off + kh * dh;
-        float* ksr = scratch_row + warp * 2 * kMaxDh;  // per-warp staging in global scratch
-        float* vsr = ksr + kMaxDh;
-        for (int i = lane; i < dh / 2; i += 32) {
-          const float a = __ldcg(kr + i), b = __ldcg(kr + i + dh / 2);
-          const float2 cs = mp ? __ldcg(md.mtp_rope + si * (kMaxDh / 2) + i) : sd.rope[row][i];
-          ksr[i] = a * cs.x - b * cs.y;
-          ksr[i + dh / 2] = a * cs.y + b * cs.x;
-        }
-        for (int d = lane; d < dh; d += 32) vsr[d] = __ldcg(vr + d);
-        __syncwarp();
-        attn_store_kv(md, fa_i, page, kh, slot, ksr, 0, newt, reinterpret_cast<__half*>(newt + SL.ks_off), SL, t,
-                      lane);
-        attn_store_kv(md, fa_i, page, kh, slot, vsr, 1, newt + SL.v_off, reinterpret_cast<__half*>(newt + SL.vs_off),
-                      SL, t, lane);
-        __syncwarp();
+        const float2* rope = mp ? md.mtp_rope + si * (kMaxDh / 2) : sd.rope[row];
+        attn_new_row(md, kr, vr, rope, fa_i, page, kh, slot, newt, SL, t, lane);
       }
     }
     math_sync();
@@ -2138,16 +2189,16 @@ __device__ __noinline__ bool attn_phase(const ModelDesc& md, const StepDesc& sd,
 // and 32-dim blocks per warp: each warp holds nq n-tiles x 2 jw m-tiles of O^T.
 template <bool Q8, bool SWZ>
 __device__ __forceinline__ bool attn_dispatch(int nq, int jw, const ModelDesc& md, const StepDesc& sd, int layer,
-                                              const Smem& sm, float* scratch_row, WarpCtx& wc, int mp) {
+                                              const Smem& sm, WarpCtx& wc, int mp) {
   switch (nq) {
     case 1:
-      if (jw == 4) return attn_phase<Q8, SWZ, 1, 4>(md, sd, layer, sm, scratch_row, wc, mp);
-      return attn_phase<Q8, SWZ, 1, 2>(md, sd, layer, sm, scratch_row, wc, mp);
-    case 2: return attn_phase<Q8, SWZ, 2, 2>(md, sd, layer, sm, scratch_row, wc, mp);
-    case 3: return attn_phase<Q8, SWZ, 3, 2>(md, sd, layer, sm, scratch_row, wc, mp);
-    case 4: return attn_phase<Q8, SWZ, 4, 1>(md, sd, layer, sm, scratch_row, wc, mp);
-    case 5: return attn_phase<Q8, SWZ, 5, 1>(md, sd, layer, sm, scratch_row, wc, mp);
-    default: return attn_phase<Q8, SWZ, 6, 1>(md, sd, layer, sm, scratch_row, wc, mp);
+      if (jw == 4) return attn_phase<Q8, SWZ, 1, 4>(md, sd, layer, sm, wc, mp);
+      return attn_phase<Q8, SWZ, 1, 2>(md, sd, layer, sm, wc, mp);
+    case 2: return attn_phase<Q8, SWZ, 2, 2>(md, sd, layer, sm, wc, mp);
+    case 3: return attn_phase<Q8, SWZ, 3, 2>(md, sd, layer, sm, wc, mp);
+    case 4: return attn_phase<Q8, SWZ, 4, 1>(md, sd, layer, sm, wc, mp);
+    case 5: return attn_phase<Q8, SWZ, 5, 1>(md, sd, layer, sm, wc, mp);
+    default: return attn_phase<Q8, SWZ, 6, 1>(md, sd, layer, sm, wc, mp);
   }
 }
 
@@ -2477,7 +2528,7 @@ __device__ __noinline__ void producer_warp(const ModelDesc& md, const StepDesc& 
 // ------------------------------------------------------------- the kernel
 // 9 warps: at most 168 registers each (three warps share a sub-partition).
 __global__ void __launch_bounds__(kLaunchThreads, 1)
-    mk_persistent(const ModelDesc* __restrict__ mdp, const StepDesc* __restrict__ sdp, float* attn_scratch,
+    mk_persistent(const ModelDesc* __restrict__ mdp, const StepDesc* __restrict__ sdp,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   __shared__ int sflag;
   const Smem sm{};
@@ -2507,7 +2558,6 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
   wc.kv_pos = 0;
 
   int nbar = 0;
-  float* my_scratch = attn_scratch + static_cast<size_t>(blockIdx.x) * kWarps * 2 * kMaxDh;
   // Phases: 0 embed; then per layer l: 1+5l input GEMM, 2+5l mixer,
   // 3+5l o_proj, 4+5l gate/up, 5+5l down; then lm_head; then verify. With an
   // MTP head, nine more per draft pass p: input rows, W_fc, input
@@ -2515,10 +2565,10 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
   const int n_main = 1 + 5 * md.n_layers + 2;
   const int n_phases = n_main + (md.has_mtp ? 9 * md.n_draft : 0);
   auto attention = [&](int layer, int mp) {
-    if (!md.kv_q8) return attn_dispatch<false, true>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, my_scratch, wc, mp);
+    if (!md.kv_q8) return attn_dispatch<false, true>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, wc, mp);
     if (md.dh % 128 == 0)
-      return attn_dispatch<true, true>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, my_scratch, wc, mp);
-    return attn_dispatch<true, false>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, my_scratch, wc, mp);
+      return attn_dispatch<true, true>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, wc, mp);
+    return attn_dispatch<true, false>(sd.attn_nq, sd.attn_jw, md, sd, layer, sm, wc, mp);
   };
   if (md.dbg_time && blockIdx.x == 0 && threadIdx.x == 0) md.dbg_time[0] = globaltimer();
   for (int ph = 0; ph < n_phases; ++ph) {
@@ -2567,9 +2617,9 @@ __global__ void __launch_bounds__(kLaunchThreads, 1)
   }
 }
 
-cudaError_t launch_persistent(const ModelDesc* md, const StepDesc* sd, float* attn_scratch, int grid,
+cudaError_t launch_persistent(const ModelDesc* md, const StepDesc* sd, int grid,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, cudaStream_t stream) {
-  void* args[] = {const_cast<ModelDesc**>(&md), const_cast<StepDesc**>(&sd), &attn_scratch,
+  void* args[] = {const_cast<ModelDesc**>(&md), const_cast<StepDesc**>(&sd),
                   const_cast<CUtensorMap*>(tm_k), const_cast<CUtensorMap*>(tm_v)};
   return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(mk_persistent), dim3(grid), dim3(kLaunchThreads),
                                      args, kSmemBytes, stream);
