@@ -340,6 +340,7 @@ def measure(args, eng, wl, workload, world, dev, torch, layers=0):
         eng.launch()
         torch.cuda.synchronize(dev)
         per_launch.append(eng.last_launch_ms())
+    timeline = phase_timeline(eng, wl, dev, torch) if args.timeline and not n_draft else None
     out_t, out_c = eng.finish()
     total_ms = max_over_ranks(world, total_ms, dev)
     ms = total_ms / args.steps
@@ -403,7 +404,28 @@ def measure(args, eng, wl, workload, world, dev, torch, layers=0):
                 "accepted_per_step": accepted / args.e2e_steps, "steps": args.e2e_steps},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
+        **({"timeline_us": timeline} if timeline else {}),
     }
+
+
+def phase_timeline(eng, wl, dev, torch, launches=5):
+    """Per-phase time of the prepared step (block 0's %globaltimer stamp at
+    the start and at the end of every phase up to lm_head, through
+    mk_debug_timeline), averaged over a few launches run after the timed ones:
+    embed, then per layer the input projections, the mixer, o_proj, gate/up
+    and down, then lm_head (GEMM and argmax; the verify phase is not stamped)."""
+    nl = wl.model["n_layers"]
+    stamps = torch.zeros(5 * nl + 8, dtype=torch.int64, device=dev)
+    eng.timeline(stamps)
+    acc = None
+    for _ in range(launches):
+        eng.launch()
+        torch.cuda.synchronize(dev)
+        d = np.diff(stamps.cpu().numpy()[: 5 * nl + 3].astype(np.float64)) / 1e3
+        acc = d if acc is None else acc + d
+    eng.timeline(None)
+    names = ["embed"] + [f"L{l}.{p}" for l in range(nl) for p in ("in", "mix", "o", "gu", "down")] + ["lm_head"]
+    return {n: round(float(v) / launches, 1) for n, v in zip(names, acc)}
 
 
 def plain_next_rows(wl, box, out_t, out_c, rng):
@@ -476,6 +498,7 @@ def run_ours(args, world, rank, local):
             "e2e": head["e2e"],
             "gpu_launches": head["gpu_launches"],
             "clocks": head["clocks"],
+            **({"timeline_us": head["timeline_us"]} if "timeline_us" in head else {}),
             "setup_s": time.perf_counter() - t_setup,
         }
         others = {n: {k: r[k] for k in ("value", "ms_per_step", "step_us", "rows_per_step", "e2e", "clocks",
@@ -507,6 +530,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="profiling stand-in: keep only the first N layers")
+    ap.add_argument("--timeline", action="store_true",
+                    help="add timeline_us: per-phase time of the step (block 0's stamps), after the timed launches")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)
