@@ -296,9 +296,22 @@ mk_status mk_debug_scratch(mk_ctx* ctx, int32_t rows, float* x, float* y, float*
  * 5*n_layers + 4 uint64 values, every following launch writes the
  * %globaltimer value (ns) at its start and when block 0 leaves the grid
  * barrier closing each phase (embed, then per layer: input GEMM, mixer,
- * o_proj, gate/up, down; then lm_head; then verify; an MTP head's draft
- * passes after verify are not stamped). NULL stops it. */
+ * o_proj, gate/up, down; then lm_head; then, with an MTP head only, verify:
+ * without one the launch ends at verify; the draft passes are not stamped).
+ * NULL stops it. */
 mk_status mk_debug_timeline(mk_ctx* ctx, uint64_t* stamps);
+
+/* Test hook: the q8 KV codec that the attention phase applies to the step's
+ * own K and V rows, on n_blocks blocks of 32 values. Per block: scale
+ * d16[b] = binary16 nearest to max|x| / 127 (ties to even), codes
+ * q[32 b + i] = round-half-even(x / d16) clamped to [-127, 127] (0 when
+ * d16 = 0); the q8 block of the KV cache as the pages' fused kernel stores it
+ * (page "Fusing the whole speculative-decoding cycle into one CUDA kernel",
+ * section "What shipped", the paged q8 KV of the model paragraph).
+ * x, q, d16: device, fp32 / int8 / binary16 bits. stream: a cudaStream_t
+ * (NULL = the legacy default stream); the call waits for it.
+ * Errors: MK_ERR_INVALID (null buffer, negative count), MK_ERR_CUDA. */
+mk_status mk_debug_q8_encode(const float* x, int64_t n_blocks, int8_t* q, uint16_t* d16, void* stream);
 
 /* Device-side timing of the last mk_step_launch in milliseconds (CUDA events
  * on the context stream); negative if unavailable. */

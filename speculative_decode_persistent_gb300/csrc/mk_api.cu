@@ -21,6 +21,7 @@ namespace mk {
 cudaError_t pack_units(const PackSrc& p, uint8_t* dst, int n_tiles, int nsb, cudaStream_t s);
 cudaError_t launch_persistent(const ModelDesc* md, const StepDesc* sd, int grid,
                               const CUtensorMap* tm_k, const CUtensorMap* tm_v, cudaStream_t stream);
+cudaError_t launch_q8_encode(const float* x, int64_t n_blocks, int8_t* q, uint16_t* d16, cudaStream_t stream);
 cudaError_t configure_persistent(int* blocks_per_sm);
 }  // namespace mk
 
@@ -683,6 +684,14 @@ mk_status mk_debug_outputs(mk_ctx* c, float* logits, float* hidden) {
   c->md_host.dbg_hidden = hidden;
   if (cudaMemcpyAsync(c->md_dev, &c->md_host, sizeof(ModelDesc), cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
       cudaStreamSynchronize(c->stream) != cudaSuccess)
+    return MK_ERR_CUDA;
+  return MK_OK;
+}
+
+mk_status mk_debug_q8_encode(const float* x, int64_t n_blocks, int8_t* q, uint16_t* d16, void* stream) {
+  if (n_blocks < 0 || (n_blocks > 0 && (!x || !q || !d16))) return MK_ERR_INVALID;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_q8_encode(x, n_blocks, q, d16, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
     return MK_ERR_CUDA;
   return MK_OK;
 }

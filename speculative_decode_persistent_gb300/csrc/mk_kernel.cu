@@ -1801,6 +1801,27 @@ __device__ __noinline__ void attn_new_row(const ModelDesc& md, const float* kr, 
   }
 }
 
+// Test hook: the q8 block codec of attn_new_row on n_blocks blocks of 32
+// floats, one warp per block (codes q[32 b + i], scales d16[b]).
+__global__ void q8_encode_kernel(const float* x, int64_t n_blocks, int8_t* q, uint16_t* d16) {
+  const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x & 31;
+  if (b >= n_blocks) return;  // whole warps: blockDim is a multiple of 32
+  const float v = x[b * 32 + lane];
+  const __half h = q8_block_scale(warp_max(fabsf(v)));
+  q[b * 32 + lane] = static_cast<int8_t>(q8_code(v, __half2float(h)));
+  if (lane == 0) d16[b] = __half_as_ushort(h);
+}
+
+cudaError_t launch_q8_encode(const float* x, int64_t n_blocks, int8_t* q, uint16_t* d16, cudaStream_t stream) {
+  constexpr int kBlock = 256;
+  const int64_t grid = (n_blocks * 32 + kBlock - 1) / kBlock;
+  if (n_blocks <= 0) return cudaSuccess;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  q8_encode_kernel<<<static_cast<unsigned>(grid), kBlock, 0, stream>>>(x, n_blocks, q, d16);
+  return cudaGetLastError();
+}
+
 // One row of K or V that an earlier phase of this launch stored into the pool
 // (an MTP draft pass reads back the positions of the catch-up rows and of the
 // passes before it), copied as stored into row t of the new-rows chunk.

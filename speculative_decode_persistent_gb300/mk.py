@@ -99,6 +99,7 @@ def _load():
         "mk_debug_timeline": (i32, [vp, vp]),
         "mk_debug_gemm_schedule": (i32, [i32, i32, i32, i32, vp, vp]),
         "mk_debug_act_bytes": (i32, [i32, i32]),
+        "mk_debug_q8_encode": (i32, [vp, ctypes.c_int64, vp, vp, vp]),
         "mk_status_str": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -115,7 +116,7 @@ EXPORTS = ["mk_packed_bytes", "mk_kv_bytes", "mk_kv_scale_bytes", "mk_gdn_state_
            "mk_step", "mk_step_prepare", "mk_step_launch", "mk_step_finish", "mk_last_drafts", "mk_commit",
            "mk_debug_outputs", "mk_last_launch_ms", "mk_debug_skip_arrival", "mk_grid_blocks",
            "mk_status_str", "mk_debug_scratch", "mk_step_io_bytes", "mk_step_static",
-           "mk_debug_timeline", "mk_debug_gemm_schedule", "mk_debug_act_bytes"]
+           "mk_debug_timeline", "mk_debug_gemm_schedule", "mk_debug_act_bytes", "mk_debug_q8_encode"]
 
 
 def gemm_schedule(n_tiles: int, nsb: int, rows: int, grid: int):
@@ -394,3 +395,17 @@ class Engine:
             self.close()
         except Exception:
             pass
+
+
+def q8_encode(x):
+    """Test hook: the device q8 KV codec on a CUDA fp32 tensor of n x 32
+    values (blocks of 32). Returns (codes int8 [n, 32], scales binary16 bits
+    as int16 [n]) as CUDA tensors."""
+    import torch
+    x = x.contiguous().view(-1, 32)
+    n = x.shape[0]
+    q = torch.empty((n, 32), dtype=torch.int8, device=x.device)
+    d = torch.empty((n,), dtype=torch.int16, device=x.device)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    _check(lib.mk_debug_q8_encode(x.data_ptr(), n, q.data_ptr(), d.data_ptr(), stream), "mk_debug_q8_encode")
+    return q, d
