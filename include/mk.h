@@ -384,6 +384,16 @@ int32_t mk_debug_gemm_schedule(int32_t n_tiles, int32_t nsb, int32_t rows, int32
  * slice of nsb_slice super-blocks at `rows` rows (must fit the kernel's
  * activation region). */
 int32_t mk_debug_act_bytes(int32_t nsb_slice, int32_t rows);
+/* Test hook, host only: the attention plan mk_step_prepare makes when the
+ * longest sequence of a step has q_rows_max query rows per kv head
+ * (T x hq/hkv, 1..48), for head dim dh and a q8 (1) or fp16 (0) pool. out
+ * (host, 12 int32) receives: query n-tiles nq, 32-dim blocks per warp jw,
+ * warps per group wpg, groups ng, staging slots per group spg, slots nslots,
+ * the exchange areas' offset in the phase region and one group's area
+ * (bytes), the phase region, one slot, the weight ring and the page list
+ * (bytes). Returns MK_OK, MK_ERR_INVALID (bad argument) or
+ * MK_ERR_UNSUPPORTED (no plan fits: the step would be refused). */
+mk_status mk_debug_attn_plan(int32_t q_rows_max, int32_t dh, int32_t q8, int32_t* out);
 const char* mk_status_str(mk_status status);
 
 #ifdef __cplusplus

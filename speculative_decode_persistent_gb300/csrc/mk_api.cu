@@ -1119,3 +1119,22 @@ extern "C" int32_t mk_debug_gemm_schedule(int32_t n_tiles, int32_t nsb, int32_t 
 }
 
 extern "C" int32_t mk_debug_act_bytes(int32_t nsb_slice, int32_t rows) { return act_bytes(nsb_slice, rows); }
+
+extern "C" mk_status mk_debug_attn_plan(int32_t q_rows_max, int32_t dh, int32_t q8, int32_t* out) {
+  if (q_rows_max < 1 || q_rows_max > kMaxQRows || dh < 64 || dh > kMaxDh || dh % 64 || !out) return MK_ERR_INVALID;
+  int32_t nq, jw, wpg, ng, spg, nslots;
+  attn_plan(q_rows_max, dh, q8 ? 1 : 0, kRingBytes, nq, jw, wpg, ng, spg, nslots);
+  out[0] = nq;
+  out[1] = jw;
+  out[2] = wpg;
+  out[3] = ng;
+  out[4] = spg;
+  out[5] = nslots;
+  out[6] = attn_xoff(nq, dh, q8 ? 1 : 0);
+  out[7] = attn_xslab(wpg, nq, q8 ? 1 : 0);
+  out[8] = kPhaseBytes;
+  out[9] = attn_slot_layout(dh, q8 ? 1 : 0).bytes;
+  out[10] = kRingBytes;
+  out[11] = kAttnPageListBytes;
+  return spg < 1 ? MK_ERR_UNSUPPORTED : MK_OK;
+}

@@ -100,6 +100,7 @@ def _load():
         "mk_debug_gemm_schedule": (i32, [i32, i32, i32, i32, vp, vp]),
         "mk_debug_act_bytes": (i32, [i32, i32]),
         "mk_debug_q8_encode": (i32, [vp, ctypes.c_int64, vp, vp, vp]),
+        "mk_debug_attn_plan": (i32, [i32, i32, i32, vp]),
         "mk_status_str": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -116,7 +117,8 @@ EXPORTS = ["mk_packed_bytes", "mk_kv_bytes", "mk_kv_scale_bytes", "mk_gdn_state_
            "mk_step", "mk_step_prepare", "mk_step_launch", "mk_step_finish", "mk_last_drafts", "mk_commit",
            "mk_debug_outputs", "mk_last_launch_ms", "mk_debug_skip_arrival", "mk_grid_blocks",
            "mk_status_str", "mk_debug_scratch", "mk_step_io_bytes", "mk_step_static",
-           "mk_debug_timeline", "mk_debug_gemm_schedule", "mk_debug_act_bytes", "mk_debug_q8_encode"]
+           "mk_debug_timeline", "mk_debug_gemm_schedule", "mk_debug_act_bytes", "mk_debug_q8_encode",
+           "mk_debug_attn_plan"]
 
 
 def gemm_schedule(n_tiles: int, nsb: int, rows: int, grid: int):
@@ -409,3 +411,14 @@ def q8_encode(x):
     stream = torch.cuda.current_stream(x.device).cuda_stream
     _check(lib.mk_debug_q8_encode(x.data_ptr(), n, q.data_ptr(), d.data_ptr(), stream), "mk_debug_q8_encode")
     return q, d
+
+
+def attn_plan(q_rows_max: int, dh: int, q8: int):
+    """Host-only test hook: the attention plan of a step (see mk_debug_attn_plan).
+    Returns (status, dict)."""
+    import numpy as np
+    out = np.zeros(12, np.int32)
+    rc = lib.mk_debug_attn_plan(q_rows_max, dh, q8, out.ctypes.data_as(vp))
+    keys = ["nq", "jw", "wpg", "ng", "spg", "nslots", "xoff", "xslab", "phase_bytes", "slot_bytes",
+            "ring_bytes", "page_list_bytes"]
+    return rc, dict(zip(keys, (int(v) for v in out)))
