@@ -1214,14 +1214,16 @@ __device__ __noinline__ void gdn_phase(const ModelDesc& md, const StepDesc& sd, 
 // rows. Splits write (m, l, acc) partials; once all of a (sequence, head)'s
 // splits have announced theirs, every split block merges its share.
 //
-// The mma work is transposed so that the head
-// dimension and the tokens are the mma's M and K: per 16-token chunk a warp
-// forms S^T = K Q^T (16 tokens x 8 query rows), updates the online softmax of
-// its 8 query rows, and accumulates O^T += V^T P^T (its share of the head
-// dims x 8 rows) in registers. Pages arrive by tensor copies issued by the
-// producer warp into staging slots (the weight ring, idle during attention);
-// the warps of a group consume one chunk each time without block barriers.
-// The step's own rows form one more chunk (causal), built by the last split.
+// The mma work is transposed so that the head dimension and the tokens are
+// the mma's M and K: per 16-token chunk, S^T = K Q^T (16 tokens x 8 query
+// rows per n-tile) and O^T += V^T P^T (head dims x 8 rows). A group of warps
+// takes one or two chunks per step; each warp owns a share of the head dims
+// for every n-tile (its S^T share, its O^T rows), the shares meet in shared
+// memory, one owner warp per n-tile takes the online-softmax step and hands
+// back P^T, with two named-barrier syncs of the group per step. Pages arrive
+// by tensor copies issued by the producer warp into staging slots (the
+// weight ring, idle during attention). The step's own rows form one more
+// chunk (causal), built by the last split.
 __device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
@@ -1848,13 +1850,14 @@ static_assert(attn_qbytes(kMaxQRows / 8, kMaxDh) + 16384 + 16 <= kPhaseBytes, "a
 // phase's flag word: the host keeps rows x partials within kAttnCombineFloats
 static_assert(kAttnBarOff + 2 * kAttnMaxSlots * 8 <= kMiscBytes, "attention mbarriers");
 
-// Every block of a (sequence, kv head) merges its share of the splits'
-// partials once all of them are written: split j takes the output float4s
-// j, j + nsplit, ... of the head's [qrows][dh/4] output. First every split's
-// (m, l) of every row goes to shared memory in one batch of loads; then per
-// row the weights 2^(m_s - M) and 1/sum(l_s w_s); then groups of 4 threads sum
-// one output float4 over the splits (each thread a quarter of them, all its
-// loads in flight) and a shuffle adds the four.
+// Every block of a (sequence, kv head) merges its share of the partials
+// (one per warp group of every split block) once all of them are written:
+// split block j takes the output float4s j, j + nblocks, ... of the head's
+// [qrows][dh/4] output. First every partial's (m, l) of every row goes to
+// shared memory in one batch of loads; then per row the weights 2^(m_s - M)
+// and 1/sum(l_s w_s); then groups of 4 threads sum one output float4 over the
+// partials (each thread a quarter of them, all its loads in flight) and a
+// shuffle adds the four.
 __device__ __noinline__ void attn_combine(const ModelDesc& md, const StepDesc& sd, int si, int kh, int nblocks,
                                           int ngroups, int qrows, int row0, int j, float* wsm) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
