@@ -295,6 +295,43 @@ class Engine:
     def seq_reset(self, seq: int):
         _check(lib.mk_seq_reset(self.ctx, seq), "mk_seq_reset")
 
+    def seq_new(self, seq: int):
+        """Install an empty sequence (no cached token) with a zero recurrent state."""
+        Sv, Cv = self.state_views()
+        if Sv is not None:
+            Sv[seq, 0].zero_()
+            Cv[seq, 0].zero_()
+            self.torch.cuda.synchronize(self.device)
+        _check(lib.mk_seq_set(self.ctx, seq, 0, None, 0), "mk_seq_set")
+
+    def clone_sequence(self, src: int, dst: int):
+        """Install sequence dst as a copy of src's committed state: the same
+        length, src's KV pages copied to the lowest free page ids, and src's
+        committed recurrent state copied to dst's state slot 0 (device copies;
+        src must have no pending step)."""
+        torch = self.torch
+        info = self.seq_get(src)
+        used = set()
+        for s in range(self.max_seqs):
+            if s != dst:
+                used.update(int(p) for p in self.seq_get(s)["pages"])
+        free = [p for p in range(self.layout.n_pages) if p not in used]
+        n = len(info["pages"])
+        if len(free) < n:
+            raise MkError(-3, "clone_sequence (no free pages)")
+        new = np.array(free[:n], np.int32)
+        if n:
+            si = torch.as_tensor(info["pages"].astype(np.int64), device=self.device)
+            di = torch.as_tensor(new.astype(np.int64), device=self.device)
+            for v in self.kv_views().values():  # [kv layers][pages][...]
+                v[:, di] = v[:, si]
+        Sv, Cv = self.state_views()
+        if Sv is not None:
+            Sv[dst, 0].copy_(Sv[src, info["slot"]])
+            Cv[dst, 0].copy_(Cv[src, info["slot"]])
+        torch.cuda.synchronize(self.device)
+        _check(lib.mk_seq_set(self.ctx, dst, info["length"], _np_ptr(new), n), "mk_seq_set")
+
     # ----------------------------------------------------------------- step
     @staticmethod
     def _rows(tokens, positions, seq_ids, flags):
