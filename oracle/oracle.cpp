@@ -28,6 +28,8 @@
  *     logits = W_lm RMSNorm(x)
  *   greedy verification: g_j = argmax(row j), accepted a = longest prefix with
  *     draft_i == g_{i-1}; emitted d_1..d_a, g_a; count = a + 1.
+ *   (sampling verification, for temperature > 0, is orc_sample_verify at the
+ *   end of this file: it works on a sequence's logits and given uniforms.)
  *   commit: L += kept rows; recurrent state <- snapshot after the last kept row;
  *     pages wholly beyond L are freed; new pages are the lowest free ids, in row
  *     order.
@@ -805,5 +807,75 @@ double orc_sigmoid(double v) { return sigmoid(v); }
 double orc_silu(double v) { return silu(v); }
 
 int orc_n_free_pages(void* h) { return static_cast<int>(static_cast<Oracle*>(h)->free_pages.size()); }
+
+/*
+ * Speculative SAMPLING verification of one sequence's T rows. Page "UPDATE:
+ * Qwen 3.8 27B 140 tok/s on single RTX 3090 Megakernel: KL divergence 0.0009
+ * vs llama.cpp", section "Decode accuracy": with sampling the output keeps the
+ * distribution of sampling without drafts; page "OpenJet's CUDA megakernel
+ * runs 4 coding agents on one RTX 3090", section "Caveats": top_k capped at
+ * 32. The drafts are single proposals (prompt-lookup or the MTP head's
+ * greedy choice), so the rule is the standard one for a draft proposed with
+ * probability 1:
+ *   p_j = softmax over the top_k largest logits of row j (ties: lower token
+ *         id first) of logits / temperature, zero elsewhere.
+ *   for i = 0 .. T-2, d = drafts[i] (the token of row i+1, proposed with
+ *   certainty): accept when u[i][0] < p_i(d); otherwise emit x drawn from
+ *   the residual p_i(x) for x != d (renormalised by 1 - p_i(d)) by inverse
+ *   CDF over ascending token ids with u[i][1], and stop.
+ *   all accepted: emit a bonus drawn from p_{T-1} with u[T-1][1].
+ * out receives the accepted drafts then the last token; returns the count
+ * (accepted + 1), or -1 on a bad argument. logits fp64 [T][V], u [T][2].
+ */
+static void topk_probs(const double* row, int V, double temperature, int top_k, std::vector<double>& p) {
+    std::vector<int> idx(V);
+    for (int x = 0; x < V; ++x) idx[x] = x;
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return row[a] > row[b]; });
+    p.assign(V, 0.0);
+    const int k = std::min(top_k, V);
+    const double m = row[idx[0]] / temperature;
+    double z = 0;
+    for (int j = 0; j < k; ++j) {
+        p[idx[j]] = std::exp(row[idx[j]] / temperature - m);
+        z += p[idx[j]];
+    }
+    for (int j = 0; j < k; ++j) p[idx[j]] /= z;
+}
+
+static int draw(const std::vector<double>& w, double total, double u) {
+    /* the first token whose running sum of w exceeds u * total */
+    double acc = 0;
+    int last = -1;
+    for (int x = 0; x < static_cast<int>(w.size()); ++x) {
+        if (w[x] <= 0) continue;
+        acc += w[x];
+        last = x;
+        if (u * total < acc) return x;
+    }
+    return last;
+}
+
+int orc_sample_verify(const double* logits, int T, int V, const int* drafts, double temperature, int top_k,
+                      const double* u, int* out) {
+    if (T < 1 || V < 1 || !(temperature > 0) || top_k < 1 || !logits || !u || !out || (T > 1 && !drafts))
+        return -1;
+    std::vector<double> p;
+    for (int i = 0; i + 1 < T; ++i) {
+        topk_probs(logits + static_cast<size_t>(i) * V, V, temperature, top_k, p);
+        const int d = drafts[i];
+        if (d < 0 || d >= V) return -1;
+        if (u[2 * i] < p[d]) {
+            out[i] = d;
+            continue;
+        }
+        const double pd = p[d];
+        p[d] = 0;
+        out[i] = draw(p, 1.0 - pd, u[2 * i + 1]);
+        return i + 1;
+    }
+    topk_probs(logits + static_cast<size_t>(T - 1) * V, V, temperature, top_k, p);
+    out[T - 1] = draw(p, 1.0, u[2 * (T - 1) + 1]);
+    return T;
+}
 
 } /* extern "C" */

@@ -75,6 +75,8 @@ def _bind(L):
     L.orc_q4_encode.argtypes = [vp, i64, vp]
     L.orc_q4_matvec.argtypes = [vp, i32, i32, vp, vp, i32]
     L.orc_q8_encode.argtypes = [vp, i64, vp, vp]
+    L.orc_sample_verify.argtypes = [vp, i32, i32, vp, dbl, i32, vp, vp]
+    L.orc_sample_verify.restype = i32
     L.orc_half_round.argtypes = [dbl]
     L.orc_half_round.restype = ctypes.c_uint16
     L.orc_half_value.argtypes = [ctypes.c_uint16]
@@ -294,6 +296,24 @@ def q8_encode(x: np.ndarray):
     d = np.zeros(x.shape[0], np.uint16)
     lib().orc_q8_encode(_p(x), x.shape[0], _p(q), _p(d))
     return q, d
+
+
+def sample_verify(logits: np.ndarray, drafts, temperature: float, top_k: int, u: np.ndarray, library=None):
+    """Speculative sampling verification of one sequence's rows (see
+    orc_sample_verify): logits [T][V], drafts [T-1], u [T][2] uniforms in
+    [0, 1). Returns the emitted tokens (accepted drafts, then the last one).
+    library: a variant built by build_variant (tests), else the oracle."""
+    logits = np.ascontiguousarray(logits, np.float64)
+    T, V = logits.shape
+    d = np.ascontiguousarray(np.asarray(drafts, np.int32).reshape(-1))
+    u = np.ascontiguousarray(u, np.float64).reshape(T, 2)
+    out = np.zeros(T, np.int32)
+    L = library if library is not None else lib()
+    n = L.orc_sample_verify(_p(logits), T, V, _p(d) if T > 1 else None, float(temperature), int(top_k),
+                            _p(u), _p(out))
+    if n < 0:
+        raise ValueError("orc_sample_verify: bad argument")
+    return [int(x) for x in out[:n]]
 
 
 def half_round(x: float) -> int:
