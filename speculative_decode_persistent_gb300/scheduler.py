@@ -101,7 +101,7 @@ class AgentScheduler:
 
     # ------------------------------------------------------------- slots
     def _free_slot(self):
-        used = {c.slot for c in self.convs.values()} | {t.slot for t in self.templates}
+        used = {c.slot for c in self.convs.values()} | {t.slot for t in self.templates if t is not None}
         for s in range(self.max_slots):
             if s not in used:
                 return s
@@ -143,7 +143,15 @@ class AgentScheduler:
             c = _Conv(cid, self._free_slot())
             tpl = self._template_for(tokens)
             if tpl is not None:
-                self.eng.clone_sequence(tpl.slot, c.slot)
+                while True:  # the copy needs free pages: idle conversations give theirs up
+                    try:
+                        self.eng.clone_sequence(tpl.slot, c.slot)
+                        break
+                    except MkError as e:
+                        idle = [x for x in self.convs.values() if not x.active()]
+                        if e.status != MK_ERR_NO_PAGES or not idle:
+                            raise
+                        self.release(min(idle, key=lambda x: x.last_used).cid)
                 c.history, c.cached = list(tpl.tokens), len(tpl.tokens)
                 tokens = tokens[len(tpl.tokens):]
             else:
@@ -157,6 +165,8 @@ class AgentScheduler:
     def _template_for(self, tokens):
         best = None
         for t in self.templates:
+            if t is None:
+                continue
             n = len(t.tokens)
             if n < len(tokens) and tokens[:n] == t.tokens and (best is None or n > len(best.tokens)):
                 best = t
@@ -166,6 +176,14 @@ class AgentScheduler:
         """Drop a conversation; its slot and pages return to the engine."""
         c = self.convs.pop(cid)
         self.eng.seq_reset(c.slot)
+
+    def drop_prefix(self, tid: int):
+        """Drop a registered prefix; its slot and pages return to the engine
+        (conversations already copied from it keep their copies)."""
+        t = self.templates[tid]
+        if t is not None:
+            self.eng.seq_reset(t.slot)
+            self.templates[tid] = None
 
     def output(self, cid):
         return list(self.convs[cid].new)

@@ -354,3 +354,24 @@ def test_scheduler_on_the_oracle_tiny_model():
     out = sch.run()
     for i, p in enumerate(prompts):
         assert out[i] == oracle_solo(make, p, 10), i
+
+
+def test_prefix_copy_evicts_idle_and_prefix_can_be_dropped():
+    rng = np.random.default_rng(23)
+    system = [int(x) for x in rng.integers(0, V, 33)]  # 3 pages once processed
+    eng = ToyEngine(n_pages=8)
+    sch = AgentScheduler(eng, n_draft=1, max_slots=4)
+    tid = sch.register_prefix(system)
+    u1 = [int(x) for x in rng.integers(0, V, 5)]
+    sch.submit("x", system + u1, 4)
+    out = sch.run()
+    assert out["x"] == solo(system + u1, 4)[0]
+    # "x" (3 pages) is idle; a second copy of the prefix needs 3 of the 2 free pages
+    u2 = [int(x) for x in rng.integers(0, V, 4)]
+    sch.submit("y", system + u2, 3)
+    assert "x" not in sch.convs
+    assert sch.run()["y"] == solo(system + u2, 3)[0]
+    sch.drop_prefix(tid)
+    assert sch.templates[tid] is None and len(eng.free) == 8 - len(eng.seqs[sch.convs["y"].slot]["pages"])
+    sch.submit("z", system + u1, 4)  # no template any more: the whole prompt is processed
+    assert sch.run()["z"] == solo(system + u1, 4)[0]
