@@ -375,3 +375,32 @@ def test_prefix_copy_evicts_idle_and_prefix_can_be_dropped():
     assert sch.templates[tid] is None and len(eng.free) == 8 - len(eng.seqs[sch.convs["y"].slot]["pages"])
     sch.submit("z", system + u1, 4)  # no template any more: the whole prompt is processed
     assert sch.run()["z"] == solo(system + u1, 4)[0]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_mixes_match_solo(seed):
+    """Random conversation mixes, row limits, draft depths and follow-ups:
+    every step stays within the engine's limits (the toy engine asserts them)
+    and every text equals the conversation decoded alone."""
+    rng = np.random.default_rng(100 + seed)
+    eng = ToyEngine(n_pages=96)
+    sch = AgentScheduler(eng, n_draft=int(rng.integers(0, 5)), max_rows=int(rng.integers(6, 13)),
+                         max_rows_per_seq=int(rng.integers(2, 9)), min_prefill_rows=int(rng.integers(1, 5)))
+    n = int(rng.integers(2, 7))
+    prompts = _prompts(rng, n, 1, 30)
+    want_new = [int(rng.integers(1, 25)) for _ in range(n)]
+    for i in range(n):
+        sch.submit(i, prompts[i], want_new[i])
+        if rng.random() < 0.5:
+            sch.step()  # arrivals spread over steps
+    first = sch.run()
+    follow = {i: (_prompts(rng, 1, 1, 8)[0], int(rng.integers(1, 10))) for i in range(n) if rng.random() < 0.5}
+    for i, (t, m) in follow.items():
+        sch.submit(i, t, m)
+    second = sch.run()
+    for i in range(n):
+        want = solo(prompts[i], want_new[i], follow=[follow[i]] if i in follow else [])
+        assert first[i] == want[0], (seed, i)
+        if i in follow:
+            assert second[i] == want[1], (seed, i)
+    assert sum(n_rows for _s, _f, n_rows in eng.rows_seen) == sch.rows_total
