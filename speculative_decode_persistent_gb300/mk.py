@@ -181,6 +181,10 @@ class Engine:
                  device: str = "cuda:0", stream=None, max_pages_per_seq: int | None = None,
                  n_state_slots: int = MK_MAX_T + 1, n_draft: int = 0):
         import torch
+        if kv_q8 and model["dh"] % 128 and model["dh"] != 64:
+            # the q8 page reader assumes one 64-byte box per K/V row when rows are
+            # not a multiple of 128 bytes: a q8 head dim of 192 is not supported
+            raise MkError(-8, "Engine (q8 KV needs a head dim of 64 or a multiple of 128)")
         self.torch = torch
         self.model = model
         self.device = torch.device(device)

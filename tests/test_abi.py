@@ -98,3 +98,12 @@ def test_mtp_layout_sizes_and_rejections(mk):
         assert mk.lib.mk_packed_bytes(ctypes.byref(bad)) == 0, kw
     bad = mk.make_layout(dict(m, draft_vocab=m["vocab"] + 1), kv_q8=0, n_pages=320, max_seqs=1, n_draft=4)
     assert mk.lib.mk_packed_bytes(ctypes.byref(bad)) == 0
+
+
+def test_engine_refuses_q8_head_dim_192():
+    from gen import configs
+    from speculative_decode_persistent_gb300 import mk
+    model = dict(configs.TINY, dh=192, hq=2, hkv=1)
+    with pytest.raises(mk.MkError) as e:
+        mk.Engine(model, {}, 1, 64)
+    assert e.value.status == -8
