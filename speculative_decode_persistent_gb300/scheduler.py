@@ -22,8 +22,9 @@ shipped" and "Why it matters"):
 
 The engine is any object with the mk.Engine calls used here: step, commit,
 seq_get, seq_reset, seq_new (an empty sequence with a zero recurrent state)
-and clone_sequence. The scheduler commits the rows it keeps right after each
-step, so no sequence is left pending between steps.
+and clone_sequence, for a model without an MTP head (the library takes no
+prompt rows beside one). The scheduler commits the rows it keeps right after
+each step, so no sequence is left pending between steps.
 """
 from __future__ import annotations
 
